@@ -1,0 +1,63 @@
+"""Planted mistakes in copies of the oracle must each fail at least one pin.
+
+Every mutant is a textual edit of ``oracle/qkv_oracle.c`` compiled into a
+temporary library on the CPU; the real oracle is never modified.  This shows
+that the pins constrain each part of the oracle: projection, frequency,
+rotation, sections, bias, cache addressing and f16 rounding.
+"""
+import os
+
+import pytest
+
+import oracle
+import oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "qkv_oracle.c")
+
+MUTANTS = {
+    "rotation_sign": ("*r0 = (float)(x0 * c - x1 * s);", "*r0 = (float)(x0 * c + x1 * s);"),
+    "cos_sin_swapped": ("const double c = cos(th), s = sin(th);",
+                        "const double c = sin(th), s = cos(th);"),
+    "interleaved_pairs": ("const int j = h * hd + d, j2 = j + half;",
+                          "const int j = h * hd + 2 * d, j2 = j + 1;"),
+    "qk_bias_dropped": ("const double x0 = y0 + (double)b0;", "const double x0 = y0;"),
+    "v_bias_dropped": ("v_out[j] = (float)(yv[j] + (double)bv[j]);", "v_out[j] = (float)(yv[j]);"),
+    "v_offset_2nkt": ("const double* yv = y + nqt + nkt;", "const double* yv = y + 2 * nkt;"),
+    "freq_exponent": ("-(2.0L * (long double)d)", "-((long double)d)"),
+    "freq_not_rounded_f32": ("return (float)v;", "return (float)(double)(v * 1.0000001L);"),
+    "kv_row_stride": ("(size_t)pos * (size_t)nkt : 0;", "(size_t)pos * (size_t)(nkt - 1) : 0;"),
+    "kv_stores_wrong_value": ("kv_put(kv_k, kv_is_f16, row + (size_t)j2, k_out[j2]);",
+                              "kv_put(kv_k, kv_is_f16, row + (size_t)j2, k_out[j]);"),
+    "f16_ties_away": ("if (frac > 0.5 || (frac == 0.5 && fmod(n, 2.0) != 0.0)) n += 1.0;",
+                      "if (frac >= 0.5) n += 1.0;"),
+    "f16_truncates": ("if (frac > 0.5 || (frac == 0.5 && fmod(n, 2.0) != 0.0)) n += 1.0;",
+                      "(void)frac;"),
+    "matvec_drops_last_bf16": ("for (int64_t c = 0; c < H; ++c) acc += oracle_bf16_value",
+                               "for (int64_t c = 0; c < H - 1; ++c) acc += oracle_bf16_value"),
+    "matvec_drops_last_f32": ("for (int64_t c = 0; c < H; ++c) acc += (double)row[c]",
+                              "for (int64_t c = 0; c + 1 < H; ++c) acc += (double)row[c]"),
+    "matvec_transposed": ("acc += (double)row[c] * (double)x[c];",
+                          "acc += (double)((const float*)W)[c * R + r] * (double)x[c];"),
+    "angle_in_double": ("return (float)((double)pos * (double)inv_freq);",
+                        "return (float)((double)pos * (double)inv_freq * (1.0 + 1e-7));"),
+    "stage_skips_k_rope": ("oracle_rope_pair(yk[j], yk[j2], bk[j], bk[j2], pos, f,",
+                           "oracle_rope_pair(yk[j], yk[j2], bk[j], bk[j2], 0, f,"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, "mutation anchor not found: update the mutant table"
+    mut_src = tmp_path / ("oracle_%s.c" % name)
+    mut_src.write_text(src.replace(old, new))
+    lib_path = oracle.build(force=True, src=str(mut_src), out=str(tmp_path / ("lib_%s.so" % name)))
+    orc = oracle.Oracle(oracle.load(lib_path))
+    failed = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(orc)
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, "planted mistake %r passed every pin" % name
