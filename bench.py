@@ -1,0 +1,403 @@
+"""Benchmark of the decode attention-input stage on GB300.
+
+Default workload: Qwen2.5-14B shape, 48 layers (0-23 concat class, 24-47
+mixed class), bf16 weights, f16 KV cache of 4096 rows, decode at position
+3254.  One step = one replay of the whole-model CUDA graph (48 fused
+projection+epilogue launches).  Metric: decode QKV layers/s (whole job) and
+achieved HBM GB/s of the projection kernel against the measured copy peak.
+
+  python bench.py [--steps K] [--warmup W] [--impl native|reference] [--workload NAME]
+  torchrun --nproc-per-node N bench.py --gpus N ...   (independent replicas per GPU)
+
+Timing: CUDA events on the replay stream around K replays, barrier and
+synchronise on both sides, max over ranks.  Every step reads 3.5 GB of
+weights, far more than the 126 MB L2, so no flush is needed between steps.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from qkv_rope_kv_gb300 import configs  # noqa: E402
+from qkv_rope_kv_gb300 import synth  # noqa: E402
+
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 126 * 1024 * 1024
+METRIC = "decode QKV layers/sec and achieved HBM GB/s (fraction of GB300 peak), 1 GPU"
+DECODE_KERNEL_SRC = os.path.join(ROOT, "qkv_rope_kv_gb300", "csrc", "decode_kernels.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", default=configs.QWEN14B.name, choices=sorted(configs.WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="bound on the oracle's CPU-baseline sample")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU-baseline leg")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="profiling captures only: run the first N layers of the workload "
+                         "(the result is not a bench number and says so)")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), \
+        int(os.environ.get("LOCAL_RANK", 0))
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_source_hash() -> str:
+    with open(DECODE_KERNEL_SRC, "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()
+
+
+def traffic_per_launch(workload_name: str):
+    """DRAM bytes per projection launch from a committed ncu capture, if the kernel source
+    is unchanged since the capture; else None."""
+    try:
+        with open(TRAFFIC_FILE) as fh:
+            t = json.load(fh)
+    except Exception:
+        return None
+    if t.get("source_sha256") != decode_source_hash():
+        return None
+    return t.get("bytes_per_launch", {}).get(workload_name)
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except FileNotFoundError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        loaded = [s for s, p in zip(sm, pw) if p > 200.0] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "power_w_max": max(pw) if pw else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+# ---------------------------------------------------------------- device model
+
+def build_model(w: configs.Workload, seed: int):
+    """Seeded weights, bias, inputs and zeroed caches for all layers, resident on the device."""
+    import torch
+    import qkv_rope_kv_gb300 as Q
+
+    dt = {"f32": Q.QKV_F32, "bf16": Q.QKV_BF16, "f16": Q.QKV_F16}
+    L = w.n_layers
+    pos = w.positions[0]
+    plans = {cls: Q.qkv_plan_create(w.hidden, w.n_head, w.n_head_kv, w.head_dim, w.theta, w.n_ctx,
+                                    w_dtype=dt[w.w_dtype], kv_dtype=dt[w.kv_dtype], layer_class=cls,
+                                    freq_scale=w.freq_scale)
+             for cls in (Q.QKV_CLASS_CONCAT, Q.QKV_CLASS_MIXED)}
+    # one input block per step: [position | pad | x of every layer], one output block [L, R]
+    x_off = 256
+    in_bytes = x_off + L * w.hidden * 4
+    inbuf = torch.zeros(in_bytes, dtype=torch.uint8, device="cuda")
+    dpos = inbuf[:4].view(torch.int32)
+    dx = inbuf[x_off:].view(torch.float32).view(L, w.hidden)
+    dout = torch.zeros(L, w.rows, dtype=torch.float32, device="cuda")
+    wt = torch.int16 if w.w_dtype == "bf16" else torch.float32
+    kvt = torch.int16 if w.kv_dtype == "f16" else torch.float32
+    host_x = np.stack([synth.hidden(seed, l, pos, w.hidden) for l in range(L)])
+    a, b = w.nqt, w.nqt + w.nkt
+    layers, keep = [], []
+    hostW = np.empty((w.rows, w.hidden), np.uint16 if w.w_dtype == "bf16" else np.float32)
+    for l in range(L):
+        synth.weight_rows(seed, l, 0, w.rows, w.hidden, w.w_dtype, out=hostW)
+        dW = torch.from_numpy(hostW.view(np.int16) if w.w_dtype == "bf16" else hostW).to("cuda")
+        db = torch.from_numpy(synth.bias(seed, l, w.rows)).to("cuda")
+        dk = torch.zeros(w.n_ctx, w.nkt, dtype=kvt, device="cuda")
+        dv = torch.zeros_like(dk)
+        o = dout[l]
+        d = dict(x=dx[l], q=o[:a], k=o[a:b], v=o[b:], kv_k=dk, kv_v=dv)
+        if l in w.mixed_layers:
+            d.update(wq=dW[:a], wk=dW[a:b], wv=dW[b:], bias_q=db[:a], bias_k=db[a:b], bias_v=db[b:])
+        else:
+            d.update(w=dW, bias=db)
+        layers.append(d)
+        keep += [dW, db, dk, dv]
+    layer_plans = [plans[Q.QKV_CLASS_MIXED if l in w.mixed_layers else Q.QKV_CLASS_CONCAT] for l in range(L)]
+    h_in = torch.zeros(in_bytes, dtype=torch.uint8).pin_memory()
+    h_in[:4].view(torch.int32)[0] = pos
+    h_in[x_off:].view(torch.float32).view(L, w.hidden).copy_(torch.from_numpy(host_x))
+    inbuf.copy_(h_in)
+    h_out = torch.empty(L, w.rows, dtype=torch.float32).pin_memory()
+    torch.cuda.synchronize()
+    return dict(plans=plans, layer_plans=layer_plans, layers=layers, keep=keep, inbuf=inbuf,
+                dpos=dpos, dx=dx, dout=dout, h_in=h_in, h_out=h_out, in_bytes=in_bytes)
+
+
+def time_replays(fn, steps: int, stream):
+    import torch
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / 1e3
+
+
+def barrier_sync(world):
+    import torch
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- CPU baseline (oracle)
+
+def oracle_layers_per_s(w: configs.Workload, seed: int, seconds: float, max_layers: int | None = None):
+    """Time the oracle (single thread, as it stands) over consecutive layers of the workload
+    until `seconds` of oracle time have been spent; weight generation is not timed."""
+    import oracle
+    orc = oracle.Oracle()
+    pos = w.positions[0]
+    done, spent = 0, 0.0
+    kk = np.zeros((w.n_ctx, w.nkt), np.float32 if w.kv_dtype == "f32" else np.uint16)
+    vv = kk.copy()
+    a, b = w.nqt, w.nqt + w.nkt
+    l = 0
+    while spent < seconds and (max_layers is None or done < max_layers):
+        layer = l % w.n_layers
+        W = synth.weight_rows(seed, layer, 0, w.rows, w.hidden, w.w_dtype)
+        bias = synth.bias(seed, layer, w.rows)
+        x = synth.hidden(seed, layer, pos, w.hidden)
+        t0 = time.perf_counter()
+        if layer in w.mixed_layers:
+            orc.decode_mixed(W[:a], W[a:b], W[b:], x, bias, w.n_head, w.n_head_kv, w.head_dim,
+                             w.theta, w.freq_scale, pos, kk, vv)
+        else:
+            orc.decode(W, x, bias, w.n_head, w.n_head_kv, w.head_dim, w.theta, w.freq_scale, pos, kk, vv)
+        spent += time.perf_counter() - t0
+        done += 1
+        l += 1
+    return done / spent, done, spent
+
+
+def reference_arm(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    seed = 0
+    # warm-up layers, then K timed "steps" of one oracle layer each
+    for _ in range(args.warmup):
+        oracle_layers_per_s(w, seed, 0.0, max_layers=1)
+    total_layers, total_s = 0, 0.0
+    for _ in range(args.steps):
+        _, n, s = oracle_layers_per_s(w, seed, 0.0, max_layers=1)
+        total_layers += n
+        total_s += s
+    value = total_layers / total_s
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "layers/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded SplitMix64/Box-Muller weights, bias, x)",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "layers/s", "cores": 1, "kind": "oracle",
+                         "sample": "%d steps x 1 layer of %s at pos %d, single-threaded C oracle "
+                                   "(double accumulation), weight generation excluded"
+                                   % (args.steps, w.name, w.positions[0])},
+        "e2e": {"value": value, "unit": "layers/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w: configs.Workload):
+    return {"workload": w.name, "layers": w.n_layers, "hidden": w.hidden,
+            "heads": "%d/%d" % (w.n_head, w.n_head_kv), "head_dim": w.head_dim,
+            "w_dtype": w.w_dtype, "kv_dtype": w.kv_dtype, "n_ctx": w.n_ctx, "pos": w.positions[0],
+            "mixed_layers": "%d-%d" % (w.mixed_layers[0], w.mixed_layers[-1]) if w.mixed_layers else "none",
+            "l2": ("inputs larger than L2: %.2f GB of weights per step" % (w.n_layers * w.w_bytes() / 1e9))
+            if w.n_layers * w.w_bytes() > 4 * L2_BYTES else "weights fit in L2 (hot)",
+            "parallelism": "replicas"}
+
+
+# ---------------------------------------------------------------- native arm
+
+def native_arm(args, w):
+    import torch
+    import qkv_rope_kv_gb300 as Q
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    Q.load()
+    seed = rank  # each replica runs its own seeded model
+    m = build_model(w, seed)
+    stream = torch.cuda.Stream()
+    graph = Q.qkv_model_graph_create(m["layer_plans"], m["layers"], m["dpos"], stream)
+    kernels = graph.kernel_count
+
+    for _ in range(max(args.warmup, 3)):
+        graph.launch(stream)
+    stream.synchronize()
+    flags, _ = Q.qkv_check_device_error(stream)
+    if flags:
+        raise RuntimeError("device status flags set during warm-up: %#x" % flags)
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    barrier_sync(world)
+    elapsed = time_replays(lambda: graph.launch(stream), args.steps, stream)
+    barrier_sync(world)
+    clk = clocks.stop()
+    elapsed = max_over_ranks(elapsed, world)
+
+    e2e = None
+    if not args.no_e2e:
+        h_in, h_out = m["h_in"], m["h_out"]
+        for _ in range(3):
+            graph.run_host(h_in, m["inbuf"], m["dout"], h_out, stream)
+        barrier_sync(world)
+        e_el = time_replays(lambda: graph.run_host(h_in, m["inbuf"], m["dout"], h_out, stream),
+                            args.steps, stream)
+        barrier_sync(world)
+        e_el = max_over_ranks(e_el, world)
+        e2e = {"value": world * w.n_layers * args.steps / e_el, "unit": "layers/s",
+               "h2d_bytes_per_step": int(m["in_bytes"]),
+               "d2h_bytes_per_step": int(h_out.numel() * 4),
+               "ms_per_step": 1e3 * e_el / args.steps,
+               "path": "qkv_model_graph_run_host: pinned host x block + position -> device, "
+                       "graph replay, q|k|v of all layers -> pinned host"}
+
+    ms = 1e3 * elapsed / args.steps
+    layers_per_s = world * w.n_layers * args.steps / elapsed
+    per_layer_s = elapsed / args.steps / w.n_layers
+    algo = w.algo_bytes_per_layer()
+    achieved = algo / per_layer_s / 1e9
+    peak, peak_kind = measured_peak()
+    traffic = traffic_per_launch(w.name)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        v, n, s = oracle_layers_per_s(w, seed, args.cpu_seconds, max_layers=w.n_layers)
+        cpu = {"value": v, "unit": "layers/s", "cores": 1, "kind": "oracle",
+               "sample": "%d consecutive layers of %s at pos %d (%.1f s of oracle time), "
+                         "single-threaded C oracle, weight generation excluded"
+                         % (n, w.name, w.positions[0], s)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": layers_per_s, "unit": "layers/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded SplitMix64/Box-Muller weights ~N(0,0.02), bias ~N(0,0.1), "
+                    "x ~N(0,1); bf16 weights widened exactly, f32 accumulate)",
+            "config": workload_config(w),
+            "hbm_gbs": achieved,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_kind": peak_kind,
+                         "frac_of_nominal_8000": achieved / NOMINAL_HBM_GBS,
+                         "traffic": traffic, "algo_bytes_per_launch": algo,
+                         "kernel": "qkv_decode_kernel (fused projection + bias/RoPE/KV-store tail)",
+                         "duration_basis": "step time / %d launches (back-to-back graph replay)" % w.n_layers},
+            "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": kernels * args.steps,
+            "launches_per_step": kernels, "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    w = configs.WORKLOADS[args.workload]
+    if args.layers is not None:
+        import dataclasses
+        w = dataclasses.replace(w, name=w.name + "-first%d-layers-profiling-only" % args.layers,
+                                n_layers=args.layers,
+                                mixed_layers=tuple(l for l in w.mixed_layers if l < args.layers))
+    if args.impl == "reference":
+        reference_arm(args, w)
+    else:
+        native_arm(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,64 @@
+"""Workload shapes of the decode QKV stage (pure data, no arithmetic).
+
+Shapes are those of Qwen2.5 0.5B / 7B / 14B attention inputs, the models the
+pages measure ("73 · D3-8 — G4 FusedQKV ported to CUDA", §2: 14B od 7168 x
+id 5120, 7B od 4608 x id 3584; "07 · The allocator: liveness, buffer reuse,
+and the KV cache", §2.5: 0.5B KV width 128).  Weights, bias and inputs are
+seeded synthetic values (``qkv_rope_kv_gb300.synth``), not trained weights.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    hidden: int
+    n_head: int
+    n_head_kv: int
+    head_dim: int
+    w_dtype: str            # "f32" or "bf16"
+    kv_dtype: str           # "f32" or "f16"
+    n_ctx: int
+    n_layers: int
+    positions: tuple        # decode positions (one step per entry)
+    mixed_layers: tuple = field(default=())  # layer indices of the mixed class
+    theta: float = 1.0e6
+    freq_scale: float = 1.0
+    nt: int = 1             # tokens per step (prefill when > 1)
+
+    @property
+    def nqt(self) -> int:
+        return self.n_head * self.head_dim
+
+    @property
+    def nkt(self) -> int:
+        return self.n_head_kv * self.head_dim
+
+    @property
+    def rows(self) -> int:
+        return self.nqt + 2 * self.nkt
+
+    def w_bytes(self) -> int:
+        return self.rows * self.hidden * (4 if self.w_dtype == "f32" else 2)
+
+    def kv_elem_bytes(self) -> int:
+        return 4 if self.kv_dtype == "f32" else 2
+
+    def algo_bytes_per_layer(self) -> int:
+        """Bytes one decode layer must move: W, x, bias read; q|k|v and one cache row per region written."""
+        return (self.w_bytes() + 4 * self.hidden + 4 * self.rows + 4 * self.rows
+                + 2 * self.nkt * self.kv_elem_bytes())
+
+
+QWEN05_SINGLE = Workload("qwen2.5-0.5b-single-layer", 896, 14, 2, 64, "f32", "f32", 512, 1, (17,))
+QWEN05_SWEEP = Workload("qwen2.5-0.5b-24layer-sweep", 896, 14, 2, 64, "f32", "f16", 2048, 24,
+                        tuple(range(128)))
+QWEN7B = Workload("qwen2.5-7b-28layer", 3584, 28, 4, 128, "bf16", "f16", 4096, 28, (1641,))
+QWEN14B = Workload("qwen2.5-14b-48layer-mixed", 5120, 40, 8, 128, "bf16", "f16", 4096, 48, (3254,),
+                   mixed_layers=tuple(range(24, 48)))
+QWEN14B_PREFILL = Workload("qwen2.5-14b-prefill-nt128", 5120, 40, 8, 128, "bf16", "f16", 4096, 48,
+                           tuple(range(128)), nt=128)
+
+WORKLOADS = {w.name: w for w in (QWEN05_SINGLE, QWEN05_SWEEP, QWEN7B, QWEN14B, QWEN14B_PREFILL)}

@@ -1,0 +1,458 @@
+// Decode (nt == 1) kernels of the attention-input stage on sm_103a.
+//
+//   qkv_decode_kernel   the projection y = W x over the q | k | v rows, one
+//                       neox pair of rows per warp, with the epilogue (bias,
+//                       RoPE, KV-cache store) in the warp's tail — one launch
+//                       per layer for both layer classes.  The same kernel in
+//                       projection-only mode writes the raw y.
+//   qkv_epilogue_kernel the epilogue alone over the flat index
+//                       nqt/2 + nkt/2 + nkt ("73 · D3-8 — G4 FusedQKV ported to
+//                       CUDA", §3.2 Excerpts A and B).
+//   qkv_chain_*         the seven-launch chain the fusion replaces (same page,
+//                       §2): kept as bitwise comparators.
+//
+// All three epilogue forms call the same device functions below, in the same
+// order of f32 operations (explicit _rn intrinsics, no contraction), so their
+// results agree bit for bit — the page's gate for the fusion (§2, "The
+// fusion's bitwise legitimacy").
+//
+// Projection design (HBM-bound: ~1 flop per weight byte against a ridge of
+// ~270 flop/B): every weight byte is read once with 16-byte non-allocating
+// loads, each lane streams a strided share of the two rows of its pair, x is
+// staged once per CTA in shared memory, and the two dot products are reduced
+// with a xor-shuffle butterfly (identical result in every lane).  A pair of
+// rows (j, j + hd/2) of one head lands in one warp, so RoPE needs no exchange
+// between warps.  Each row is reduced by the same code whatever class the
+// layer has, so a concat layer and the same rows split into wq / wk / wv give
+// identical bits (same page, §2, "Why the concat matmul is bitwise").
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "qkv_internal.h"
+
+namespace {
+
+constexpr int kUnroll = 4;  // 16-byte loads in flight per lane per row
+
+// Device status word: [0] flags (bit 0 = position out of range), [1] a bad position.
+__device__ unsigned int g_qkv_status[2];
+
+// ---------------------------------------------------------------- PTX helpers
+
+// Programmatic dependent launch.  Without the launch attribute both are no-ops.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// 16-byte weight load: read-only for the kernel's lifetime, streamed once,
+// so it bypasses L1 allocation.
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// ---------------------------------------------------------------- epilogue math
+
+// Angle of pair index d at position pos: the f32 product pos * inv_freq[d].
+__device__ __forceinline__ float rope_theta(int pos, float inv_freq) {
+    return __fmul_rn(__int2float_rn(pos), inv_freq);
+}
+
+// Neox rotation of the pair (x0, x1) = (element d, element d + hd/2).
+__device__ __forceinline__ void rope_rotate(float x0, float x1, float theta, float& r0, float& r1) {
+    float s, c;
+    sincosf(theta, &s, &c);
+    r0 = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, s));
+    r1 = __fadd_rn(__fmul_rn(x0, s), __fmul_rn(x1, c));
+}
+
+// Cache element store at flat index pos * nkt + j (f32, or f16 round-to-nearest-even).
+__device__ __forceinline__ void kv_put(void* kv, int f16, size_t idx, float v) {
+    if (f16) reinterpret_cast<__half*>(kv)[idx] = __float2half_rn(v);
+    else reinterpret_cast<float*>(kv)[idx] = v;
+}
+
+__device__ __forceinline__ bool pos_ok(int pos, int n_ctx) { return pos >= 0 && pos < n_ctx; }
+
+__device__ __forceinline__ void flag_bad_pos(int pos) {
+    atomicOr(&g_qkv_status[0], 1u);
+    atomicExch(&g_qkv_status[1], static_cast<unsigned int>(pos));
+}
+
+// q (sec 0) or k (sec 1) pair: bias, rotate, write back; k also goes to the cache.
+__device__ __forceinline__ void epi_qk_pair(const DecodeParams& p, int sec, int j, int j2, float y0,
+                                            float y1, int pos, float inv_freq, bool store) {
+    const float* b = p.bias[sec];
+    const float x0 = __fadd_rn(y0, b[j]);
+    const float x1 = __fadd_rn(y1, b[j2]);
+    float r0, r1;
+    rope_rotate(x0, x1, rope_theta(pos, inv_freq), r0, r1);
+    float* o = p.out[sec];
+    o[j] = r0;
+    o[j2] = r1;
+    if (sec == 1 && store) {
+        const size_t row = static_cast<size_t>(pos) * static_cast<size_t>(p.nkt);
+        kv_put(p.kv_k, p.kv_f16, row + j, r0);
+        kv_put(p.kv_k, p.kv_f16, row + j2, r1);
+    }
+}
+
+// v element: bias, write back, store to the cache.
+__device__ __forceinline__ void epi_v_elem(const DecodeParams& p, int j, float y, int pos, bool store) {
+    const float val = __fadd_rn(y, p.bias[2][j]);
+    p.out[2][j] = val;
+    if (store) kv_put(p.kv_v, p.kv_f16, static_cast<size_t>(pos) * static_cast<size_t>(p.nkt) + j, val);
+}
+
+// ---------------------------------------------------------------- projection
+
+// Unit u -> (section, row pair, pair index d).  q and k units are the neox pairs
+// (h*hd + d, h*hd + d + hd/2); v units are adjacent rows (2u', 2u' + 1).
+__device__ __forceinline__ void unit_rows(int u, int qpairs, int kpairs, int half, int hd, int& sec,
+                                          int& r0, int& r1, int& d) {
+    if (u < qpairs + kpairs) {
+        sec = (u < qpairs) ? 0 : 1;
+        const int v = (u < qpairs) ? u : u - qpairs;
+        const int h = v / half;
+        d = v - h * half;
+        r0 = h * hd + d;
+        r1 = r0 + half;
+    } else {
+        sec = 2;
+        d = 0;
+        r0 = 2 * (u - qpairs - kpairs);
+        r1 = r0 + 1;
+    }
+}
+
+// acc += sum of 8 bf16 weights (one 16-byte chunk) times x[8c .. 8c+7].
+__device__ __forceinline__ float fma_chunk_bf16(uint4 w, float4 xa, float4 xb, float acc) {
+    acc = __fmaf_rn(bf16_lo(w.x), xa.x, acc);
+    acc = __fmaf_rn(bf16_hi(w.x), xa.y, acc);
+    acc = __fmaf_rn(bf16_lo(w.y), xa.z, acc);
+    acc = __fmaf_rn(bf16_hi(w.y), xa.w, acc);
+    acc = __fmaf_rn(bf16_lo(w.z), xb.x, acc);
+    acc = __fmaf_rn(bf16_hi(w.z), xb.y, acc);
+    acc = __fmaf_rn(bf16_lo(w.w), xb.z, acc);
+    acc = __fmaf_rn(bf16_hi(w.w), xb.w, acc);
+    return acc;
+}
+
+// acc += sum of 4 f32 weights times x[4c .. 4c+3].
+__device__ __forceinline__ float fma_chunk_f32(uint4 w, float4 x, float acc) {
+    acc = __fmaf_rn(__uint_as_float(w.x), x.x, acc);
+    acc = __fmaf_rn(__uint_as_float(w.y), x.y, acc);
+    acc = __fmaf_rn(__uint_as_float(w.z), x.z, acc);
+    acc = __fmaf_rn(__uint_as_float(w.w), x.w, acc);
+    return acc;
+}
+
+// Per-lane partial dot products of two rows with the staged x.  Lane l takes
+// 16-byte chunks l, l + 32, l + 64, ... in increasing order.
+//   bf16 rows: x staged as two planes of float4 (x[8c..8c+3], x[8c+4..8c+7]) so a
+//              warp's shared loads are contiguous.
+//   f32 rows:  x staged as float4 x[4c..4c+3].
+template <typename WT>
+__device__ __forceinline__ void dot2_vec(const WT* row0, const WT* row1, const float4* xs, int H,
+                                         int lane, float& a0, float& a1) {
+    constexpr bool kBf16 = sizeof(WT) == 2;
+    constexpr int kPerChunk = kBf16 ? 8 : 4;
+    const int nch = H / kPerChunk;
+    const uint4* w0 = reinterpret_cast<const uint4*>(row0);
+    const uint4* w1 = reinterpret_cast<const uint4*>(row1);
+    const float4* xb = xs + nch;  // second plane (bf16 only)
+    a0 = 0.f;
+    a1 = 0.f;
+    int c = lane;
+    for (; c + 32 * (kUnroll - 1) < nch; c += 32 * kUnroll) {
+        uint4 v0[kUnroll], v1[kUnroll];
+#pragma unroll
+        for (int i = 0; i < kUnroll; ++i) {
+            v0[i] = ld_stream(w0 + c + 32 * i);
+            v1[i] = ld_stream(w1 + c + 32 * i);
+        }
+#pragma unroll
+        for (int i = 0; i < kUnroll; ++i) {
+            const int cc = c + 32 * i;
+            if constexpr (kBf16) {
+                const float4 xa = xs[cc], xb2 = xb[cc];
+                a0 = fma_chunk_bf16(v0[i], xa, xb2, a0);
+                a1 = fma_chunk_bf16(v1[i], xa, xb2, a1);
+            } else {
+                const float4 xv = xs[cc];
+                a0 = fma_chunk_f32(v0[i], xv, a0);
+                a1 = fma_chunk_f32(v1[i], xv, a1);
+            }
+        }
+    }
+    for (; c < nch; c += 32) {
+        const uint4 v0 = ld_stream(w0 + c), v1 = ld_stream(w1 + c);
+        if constexpr (kBf16) {
+            const float4 xa = xs[c], xb2 = xb[c];
+            a0 = fma_chunk_bf16(v0, xa, xb2, a0);
+            a1 = fma_chunk_bf16(v1, xa, xb2, a1);
+        } else {
+            const float4 xv = xs[c];
+            a0 = fma_chunk_f32(v0, xv, a0);
+            a1 = fma_chunk_f32(v1, xv, a1);
+        }
+    }
+}
+
+template <typename WT>
+__device__ __forceinline__ float w_value(const WT* row, int i);
+template <>
+__device__ __forceinline__ float w_value<float>(const float* row, int i) {
+    return __ldg(row + i);
+}
+template <>
+__device__ __forceinline__ float w_value<uint16_t>(const uint16_t* row, int i) {
+    return __uint_as_float(static_cast<uint32_t>(__ldg(row + i)) << 16);
+}
+
+// Scalar path for rows that are not 16-byte aligned: lane l takes elements
+// l, l + 32, ... in increasing order; x staged plainly.
+template <typename WT>
+__device__ __forceinline__ void dot2_scalar(const WT* row0, const WT* row1, const float* xs, int H,
+                                            int lane, float& a0, float& a1) {
+    a0 = 0.f;
+    a1 = 0.f;
+    for (int i = lane; i < H; i += 32) {
+        const float xv = xs[i];
+        a0 = __fmaf_rn(w_value(row0, i), xv, a0);
+        a1 = __fmaf_rn(w_value(row1, i), xv, a1);
+    }
+}
+
+// Stage x (and the frequency table) in shared memory.
+template <typename WT, bool VEC>
+__device__ __forceinline__ void stage_x(const DecodeParams& p, float4* xs4, float* freq_s) {
+    const int H = p.H;
+    if constexpr (VEC && sizeof(WT) == 2) {
+        const int nch = H / 8;
+        const float4* xg = reinterpret_cast<const float4*>(p.x);
+        for (int c = threadIdx.x; c < nch; c += blockDim.x) {
+            xs4[c] = xg[2 * c];
+            xs4[nch + c] = xg[2 * c + 1];
+        }
+    } else if constexpr (VEC) {
+        const int nch = H / 4;
+        const float4* xg = reinterpret_cast<const float4*>(p.x);
+        for (int c = threadIdx.x; c < nch; c += blockDim.x) xs4[c] = xg[c];
+    } else {
+        float* xs = reinterpret_cast<float*>(xs4);
+        for (int i = threadIdx.x; i < H; i += blockDim.x) xs[i] = p.x[i];
+    }
+    for (int i = threadIdx.x; i < (p.hd >> 1); i += blockDim.x) freq_s[i] = p.inv_freq[i];
+}
+
+template <typename WT, bool VEC, int MODE>
+__global__ void __launch_bounds__(256) qkv_decode_kernel(const __grid_constant__ DecodeParams p) {
+    extern __shared__ float4 smem4[];
+    __shared__ float freq_s[QKV_MAX_HEAD_DIM / 2];
+    const int lane = threadIdx.x & 31;
+    const int wpc = blockDim.x >> 5;
+    const int gwarp = blockIdx.x * wpc + (threadIdx.x >> 5);
+    const int nwarps = gridDim.x * wpc;
+    const int half = p.hd >> 1;
+    const int qpairs = p.nqt >> 1, kpairs = p.nkt >> 1;
+    const int units = qpairs + kpairs + (p.nkt >> 1);
+
+    // Inputs written upstream (x, pos) are read, and outputs written, only
+    // after the preceding grid in the stream has completed.
+    griddep_wait();
+    stage_x<WT, VEC>(p, smem4, freq_s);
+    __syncthreads();
+    const int pos = (MODE == kFused) ? *p.pos : 0;
+    const bool store = pos_ok(pos, p.n_ctx);
+    griddep_launch_dependents();
+    if (MODE == kFused && !store && blockIdx.x == 0 && threadIdx.x == 0) flag_bad_pos(pos);
+
+    for (int u = gwarp; u < units; u += nwarps) {
+        int sec, r0, r1, d;
+        unit_rows(u, qpairs, kpairs, half, p.hd, sec, r0, r1, d);
+        const WT* w = static_cast<const WT*>(p.w[sec]);
+        const size_t H = static_cast<size_t>(p.H);
+        float a0, a1;
+        if constexpr (VEC) dot2_vec<WT>(w + r0 * H, w + r1 * H, smem4, p.H, lane, a0, a1);
+        else dot2_scalar<WT>(w + r0 * H, w + r1 * H, reinterpret_cast<const float*>(smem4), p.H, lane, a0, a1);
+        a0 = warp_sum(a0);
+        a1 = warp_sum(a1);
+        if (lane == 0) {
+            if constexpr (MODE == kProjectOnly) {
+                p.out[sec][r0] = a0;
+                p.out[sec][r1] = a1;
+            } else if (sec < 2) {
+                epi_qk_pair(p, sec, r0, r1, a0, a1, pos, freq_s[d], store);
+            } else {
+                epi_v_elem(p, r0, a0, pos, store);
+                epi_v_elem(p, r1, a1, pos, store);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- standalone epilogue
+
+// One thread per unit of the flat index: q pairs, then k pairs, then v elements.
+__global__ void __launch_bounds__(256) qkv_epilogue_kernel(const __grid_constant__ DecodeParams p) {
+    __shared__ float freq_s[QKV_MAX_HEAD_DIM / 2];
+    for (int i = threadIdx.x; i < (p.hd >> 1); i += blockDim.x) freq_s[i] = p.inv_freq[i];
+    griddep_wait();
+    __syncthreads();
+    const int half = p.hd >> 1;
+    const int qpairs = p.nqt >> 1, kpairs = p.nkt >> 1;
+    const int total = qpairs + kpairs + p.nkt;
+    const int u = blockIdx.x * blockDim.x + threadIdx.x;
+    const int pos = *p.pos;
+    const bool store = pos_ok(pos, p.n_ctx);
+    if (!store && u == 0) flag_bad_pos(pos);
+    if (u >= total) return;
+    if (u < qpairs + kpairs) {
+        const int sec = (u < qpairs) ? 0 : 1;
+        const int v = (u < qpairs) ? u : u - qpairs;
+        const int h = v / half;
+        const int d = v - h * half;
+        const int j = h * p.hd + d, j2 = j + half;
+        const float* io = p.out[sec];
+        epi_qk_pair(p, sec, j, j2, io[j], io[j2], pos, freq_s[d], store);
+    } else {
+        const int j = u - qpairs - kpairs;
+        epi_v_elem(p, j, p.out[2][j], pos, store);
+    }
+}
+
+// ---------------------------------------------------------------- unfused chain
+
+__global__ void qkv_chain_add_bias_kernel(float* y, const float* b, int64_t n) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i < n) y[i] = __fadd_rn(y[i], b[i]);
+}
+
+__global__ void qkv_chain_rope_kernel(const __grid_constant__ DecodeParams p, float* y, int n_heads) {
+    const int half = p.hd >> 1;
+    const int u = blockIdx.x * blockDim.x + threadIdx.x;
+    if (u >= n_heads * half) return;
+    const int h = u / half, d = u - h * half;
+    const int j = h * p.hd + d, j2 = j + half;
+    const int pos = *p.pos;
+    float r0, r1;
+    rope_rotate(y[j], y[j2], rope_theta(pos, p.inv_freq[d]), r0, r1);
+    y[j] = r0;
+    y[j2] = r1;
+}
+
+__global__ void qkv_chain_store_kernel(const __grid_constant__ DecodeParams p, const float* src, void* cache) {
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    const int pos = *p.pos;
+    const bool store = pos_ok(pos, p.n_ctx);
+    if (!store && j == 0) flag_bad_pos(pos);
+    if (j >= p.nkt || !store) return;
+    kv_put(cache, p.kv_f16, static_cast<size_t>(pos) * static_cast<size_t>(p.nkt) + j, src[j]);
+}
+
+// ---------------------------------------------------------------- launch helpers
+
+template <typename K>
+cudaError_t launch_ex(K kernel, dim3 grid, dim3 block, size_t smem, bool pdl, cudaStream_t stream,
+                      const DecodeParams& p) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+template <typename WT, bool VEC, int MODE>
+cudaError_t launch_decode_t(const DecodeParams& p, bool pdl, cudaStream_t stream) {
+    auto kernel = qkv_decode_kernel<WT, VEC, MODE>;
+    const size_t smem = static_cast<size_t>(p.H) * sizeof(float);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    const int units = (p.nqt >> 1) + (p.nkt >> 1) + (p.nkt >> 1);
+    // Small layers: 4-warp CTAs spread the rows over more SMs.
+    const int wpc = (units >= 8 * 152) ? 8 : 4;
+    const int grid = (units + wpc - 1) / wpc;
+    return launch_ex(kernel, dim3(grid), dim3(wpc * 32), smem, pdl, stream, p);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeParams& p, int w_dtype, int vec, DecodeMode mode, bool pdl,
+                          cudaStream_t stream) {
+    if (w_dtype == QKV_BF16) {
+        if (vec) return mode == kFused ? launch_decode_t<uint16_t, true, kFused>(p, pdl, stream)
+                                       : launch_decode_t<uint16_t, true, kProjectOnly>(p, pdl, stream);
+        return mode == kFused ? launch_decode_t<uint16_t, false, kFused>(p, pdl, stream)
+                              : launch_decode_t<uint16_t, false, kProjectOnly>(p, pdl, stream);
+    }
+    if (vec) return mode == kFused ? launch_decode_t<float, true, kFused>(p, pdl, stream)
+                                   : launch_decode_t<float, true, kProjectOnly>(p, pdl, stream);
+    return mode == kFused ? launch_decode_t<float, false, kFused>(p, pdl, stream)
+                          : launch_decode_t<float, false, kProjectOnly>(p, pdl, stream);
+}
+
+cudaError_t launch_epilogue(const DecodeParams& p, cudaStream_t stream) {
+    const int total = (p.nqt >> 1) + (p.nkt >> 1) + p.nkt;
+    const int grid = (total + 255) / 256;
+    return launch_ex(qkv_epilogue_kernel, dim3(grid), dim3(256), 0, false, stream, p);
+}
+
+cudaError_t launch_chain_add_bias(float* y, const float* b, int64_t n, cudaStream_t stream) {
+    const int64_t grid = (n + 255) / 256;
+    qkv_chain_add_bias_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(y, b, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_chain_rope(const DecodeParams& p, float* y, int n_heads, cudaStream_t stream) {
+    const int total = n_heads * (p.hd >> 1);
+    qkv_chain_rope_kernel<<<(total + 255) / 256, 256, 0, stream>>>(p, y, n_heads);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_chain_store(const DecodeParams& p, const float* src, void* cache, cudaStream_t stream) {
+    qkv_chain_store_kernel<<<(p.nkt + 255) / 256, 256, 0, stream>>>(p, src, cache);
+    return cudaGetLastError();
+}
+
+cudaError_t device_status_read(cudaStream_t stream, uint32_t* flags, int32_t* bad_pos) {
+    unsigned int h[2] = {0u, 0u};
+    cudaError_t e = cudaMemcpyFromSymbolAsync(h, g_qkv_status, sizeof(h), 0, cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return e;
+    if (h[0] != 0u) {
+        const unsigned int zero[2] = {0u, 0u};
+        e = cudaMemcpyToSymbolAsync(g_qkv_status, zero, sizeof(zero), 0, cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess) return e;
+        e = cudaStreamSynchronize(stream);
+        if (e != cudaSuccess) return e;
+    }
+    *flags = h[0];
+    *bad_pos = static_cast<int32_t>(h[1]);
+    return cudaSuccess;
+}

@@ -1,0 +1,55 @@
+// Internal declarations shared by the C-ABI layer and the kernel files of
+// libqkv.so.  Not part of the public interface (include/qkv.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "qkv.h"
+
+struct qkv_plan {
+    qkv_plan_desc d;
+    int64_t nqt, nkt, rows, half;
+    int vec;  // rows can be streamed as aligned 16-byte vectors (H * elem % 16 == 0)
+    float inv_freq[QKV_MAX_HEAD_DIM / 2];
+};
+
+// Everything one decode-layer launch needs, passed by value (__grid_constant__),
+// so a captured graph node carries its own copy.
+struct DecodeParams {
+    const float* x;         // [H] hidden vector
+    const void* w[3];       // q / k / v weight sections, row-major [rows x H]
+    const float* bias[3];   // q / k / v bias sections (fused and epilogue modes)
+    float* out[3];          // q / k / v outputs (in-place epilogue operands)
+    void* kv_k;             // K region [n_ctx x nkt]
+    void* kv_v;             // V region [n_ctx x nkt]
+    const int32_t* pos;     // device position
+    int32_t H, nqt, nkt, hd, n_ctx, kv_f16;
+    float inv_freq[QKV_MAX_HEAD_DIM / 2];
+};
+
+enum DecodeMode { kProjectOnly = 0, kFused = 1 };
+
+// decode_kernels.cu
+cudaError_t launch_decode(const DecodeParams& p, int w_dtype, int vec, DecodeMode mode, bool pdl,
+                          cudaStream_t stream);
+cudaError_t launch_epilogue(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_chain_add_bias(float* y, const float* b, int64_t n, cudaStream_t stream);
+cudaError_t launch_chain_rope(const DecodeParams& p, float* y, int n_heads, cudaStream_t stream);
+cudaError_t launch_chain_store(const DecodeParams& p, const float* src, void* cache,
+                               cudaStream_t stream);
+cudaError_t device_status_read(cudaStream_t stream, uint32_t* flags, int32_t* bad_pos);
+
+// prefill_tcgen05.cu
+struct PrefillParams {
+    const uint16_t* X;      // [nt x H] bf16
+    const uint16_t* W;      // [R x H] bf16
+    const float* bias;      // [R]
+    const int32_t* positions;
+    float* Y;               // [nt x R]
+    void* kv_k;
+    void* kv_v;
+    int32_t nt, H, nqt, nkt, hd, n_ctx, kv_f16;
+    float inv_freq[QKV_MAX_HEAD_DIM / 2];
+};
+qkv_status launch_prefill(const PrefillParams& p, cudaStream_t stream, const char** why);

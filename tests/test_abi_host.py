@@ -1,0 +1,155 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every entry
+point include/qkv.h declares, validates arguments before touching CUDA, and its
+size arithmetic matches the numbers printed on the pages."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle_pins as pins
+import qkv_rope_kv_gb300 as q
+from qkv_rope_kv_gb300 import configs
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return q.load()
+
+
+def _desc(**kw):
+    base = dict(hidden=5120, n_head=40, n_head_kv=8, head_dim=128, theta=1e6, freq_scale=1.0,
+                n_ctx=4096, w_dtype=q.QKV_BF16, kv_dtype=q.QKV_F16,
+                layer_class=q.QKV_CLASS_CONCAT, rope=q.QKV_ROPE_NEOX)
+    base.update(kw)
+    return q.qkv_plan_desc(**base)
+
+
+def _create(lib, d):
+    h = ctypes.c_void_p()
+    st = lib.qkv_plan_create(ctypes.byref(d), ctypes.byref(h))
+    if st == 0:
+        lib.qkv_plan_destroy(h)
+    return st
+
+
+def test_exports_every_declared_entry_point(lib):
+    names = q.header_entry_points()
+    assert len(names) >= 20
+    for n in names:
+        assert hasattr(lib, n), n
+    assert lib.qkv_abi_version() == 1
+    assert lib.qkv_status_str(3) == b"QKV_ERR_POS_RANGE"
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(), q.QKV_OK),
+    (dict(hidden=0), q.QKV_ERR_INVALID_ARG),
+    (dict(n_head=0), q.QKV_ERR_INVALID_ARG),
+    (dict(n_ctx=0), q.QKV_ERR_INVALID_ARG),
+    (dict(theta=0.0), q.QKV_ERR_INVALID_ARG),
+    (dict(theta=float("nan")), q.QKV_ERR_INVALID_ARG),
+    (dict(freq_scale=-1.0), q.QKV_ERR_INVALID_ARG),
+    (dict(layer_class=5), q.QKV_ERR_INVALID_ARG),
+    (dict(rope=7), q.QKV_ERR_INVALID_ARG),
+    (dict(rope=q.QKV_ROPE_INTERLEAVED), q.QKV_ERR_UNSUPPORTED),
+    (dict(head_dim=127), q.QKV_ERR_UNSUPPORTED),
+    (dict(head_dim=258), q.QKV_ERR_UNSUPPORTED),
+    (dict(w_dtype=q.QKV_F16), q.QKV_ERR_UNSUPPORTED),
+    (dict(kv_dtype=q.QKV_BF16), q.QKV_ERR_UNSUPPORTED),
+    (dict(hidden=60000), q.QKV_ERR_UNSUPPORTED),
+    (dict(hidden=7, head_dim=2, n_head=1, n_head_kv=1), q.QKV_OK),
+])
+def test_plan_validation(lib, kw, status):
+    assert _create(lib, _desc(**kw)) == status
+
+
+def test_plan_create_null_args(lib):
+    h = ctypes.c_void_p()
+    assert lib.qkv_plan_create(None, ctypes.byref(h)) == q.QKV_ERR_INVALID_ARG
+    assert lib.qkv_plan_create(ctypes.byref(_desc()), None) == q.QKV_ERR_INVALID_ARG
+    assert b"null" in lib.qkv_last_error()
+
+
+def test_sizes_match_pages():
+    shapes = {"qwen2.5-14b": configs.QWEN14B, "qwen2.5-7b": configs.QWEN7B}
+    for row in pins.read_golden("pages_shapes.txt"):
+        if row[0] == "units":
+            w = shapes[row[1]]
+            p = q.qkv_plan_create(w.hidden, w.n_head, w.n_head_kv, w.head_dim, w.theta, w.n_ctx)
+            assert p.info.epilogue_units == int(row[2])
+        elif row[0] == "concat_shape":
+            w = shapes[row[1]]
+            p = q.qkv_plan_create(w.hidden, w.n_head, w.n_head_kv, w.head_dim, w.theta, w.n_ctx)
+            assert p.info.rows == int(row[2]) and w.hidden == int(row[3])
+        elif row[0] == "kv_layer_bytes":
+            nkt, n_ctx, total = (int(v) for v in row[2:5])
+            p = q.qkv_plan_create(896, 14, 2, 64, 1e6, n_ctx, w_dtype=q.QKV_F32, kv_dtype=q.QKV_F32)
+            assert p.info.nkt == nkt
+            view = q.kv_cache_view(p, 0x1000, 0x2000)
+            assert 2 * view.region_bytes == total
+            assert view.row_stride_elems == nkt and view.k == 0x1000 and view.v == 0x2000
+        elif row[0] == "ledger":
+            # our launches per decode layer: one for both classes (page: 2 concat, 4 mixed)
+            if row[1] in ("concat", "mixed"):
+                p = q.qkv_plan_create(5120, 40, 8, 128, 1e6, 4096)
+                assert p.info.launches_decode == 1 < int(row[2])
+
+
+def test_algorithmic_bytes_match_workload_table():
+    for w in (configs.QWEN05_SINGLE, configs.QWEN7B, configs.QWEN14B):
+        p = q.qkv_plan_create(w.hidden, w.n_head, w.n_head_kv, w.head_dim, w.theta, w.n_ctx,
+                              w_dtype=q.QKV_F32 if w.w_dtype == "f32" else q.QKV_BF16,
+                              kv_dtype=q.QKV_F32 if w.kv_dtype == "f32" else q.QKV_F16)
+        assert p.info.algo_bytes_decode == w.algo_bytes_per_layer()
+    assert configs.QWEN14B.algo_bytes_per_layer() == 73_482_240
+    assert configs.QWEN7B.algo_bytes_per_layer() == 33_083_392
+
+
+def test_frequency_table_matches_oracle(orc):
+    for (H, nh, nkv, hd, theta) in ((896, 14, 2, 64, 1e6), (5120, 40, 8, 128, 1e6), (64, 2, 1, 4, 1e4)):
+        p = q.qkv_plan_create(H, nh, nkv, hd, theta, 16)
+        assert np.array_equal(p.inv_freq().view(np.uint32),
+                              orc.inv_freq_table(hd, theta, 1.0).view(np.uint32))
+
+
+def test_null_pointers_rejected_before_cuda(lib):
+    p = q.qkv_plan_create(64, 2, 1, 8, 1e4, 16)
+    with pytest.raises(q.QkvError) as e:
+        q.qkv_decode_step(p, None, 16, 16, 16, 16, 16, 16, 16, 16, stream=0)
+    assert e.value.status == q.QKV_ERR_INVALID_ARG
+    with pytest.raises(q.QkvError) as e:
+        q.qkv_epilogue(p, 16, 16, 16, 16, 16, 16, None, 16, 16, stream=0)
+    assert e.value.status == q.QKV_ERR_INVALID_ARG
+
+
+def test_class_mismatch_rejected(lib):
+    mixed = q.qkv_plan_create(64, 2, 1, 8, 1e4, 16, layer_class=q.QKV_CLASS_MIXED)
+    concat = q.qkv_plan_create(64, 2, 1, 8, 1e4, 16)
+    with pytest.raises(q.QkvError) as e:
+        q.qkv_decode_step(mixed, 16, 16, 16, 16, 16, 16, 16, 16, 16, stream=0)
+    assert e.value.status == q.QKV_ERR_INVALID_ARG
+    with pytest.raises(q.QkvError) as e:
+        q.qkv_decode_step_mixed(concat, *([16] * 13), stream=0)
+    assert e.value.status == q.QKV_ERR_INVALID_ARG
+
+
+def test_prefill_guards(lib):
+    f32 = q.qkv_plan_create(64, 2, 1, 8, 1e4, 16, w_dtype=q.QKV_F32)
+    with pytest.raises(q.QkvError) as e:
+        q.qkv_prefill_step(f32, 16, 4, 16, 16, 16, 16, 16, 16, stream=0)
+    assert e.value.status == q.QKV_ERR_UNSUPPORTED
+    mixed = q.qkv_plan_create(64, 2, 1, 8, 1e4, 16, layer_class=q.QKV_CLASS_MIXED)
+    with pytest.raises(q.QkvError) as e:
+        q.qkv_prefill_step(mixed, 16, 4, 16, 16, 16, 16, 16, 16, stream=0)
+    assert e.value.status == q.QKV_ERR_UNSUPPORTED
+
+
+def test_graph_create_guards(lib):
+    p = q.qkv_plan_create(64, 2, 1, 8, 1e4, 16)
+    h = ctypes.c_void_p()
+    plans = (ctypes.c_void_p * 1)(p.handle)
+    layers = (q.qkv_layer_ptrs * 1)()
+    assert lib.qkv_model_graph_create(plans, 0, layers, 16, 16, ctypes.byref(h)) == q.QKV_ERR_INVALID_ARG
+    assert lib.qkv_model_graph_create(plans, 1, layers, 16, None, ctypes.byref(h)) == q.QKV_ERR_INVALID_ARG
+    # layer 0 has null pointers: rejected before any capture starts
+    assert lib.qkv_model_graph_create(plans, 1, layers, 16, 16, ctypes.byref(h)) == q.QKV_ERR_INVALID_ARG
