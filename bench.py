@@ -44,7 +44,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default=configs.QWEN14B.name, choices=sorted(configs.WORKLOADS))
@@ -237,7 +237,7 @@ def oracle_layers_per_s(w: configs.Workload, seed: int, seconds: float, max_laye
     vv = kk.copy()
     a, b = w.nqt, w.nqt + w.nkt
     l = 0
-    while spent < seconds and (max_layers is None or done < max_layers):
+    while (done == 0 or spent < seconds) and (max_layers is None or done < max_layers):
         layer = l % w.n_layers
         W = synth.weight_rows(seed, layer, 0, w.rows, w.hidden, w.w_dtype)
         bias = synth.bias(seed, layer, w.rows)

@@ -66,6 +66,87 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// ---------------------------------------------------------------- mbarrier / bulk copy
+
+constexpr uint64_t kWaitTimeoutNs = 500ull * 1000ull * 1000ull;  // 0.5 s: far beyond any healthy wait
+constexpr unsigned int kFlagPosRange = 1u;
+constexpr unsigned int kFlagTimeout = 2u;
+// A waiting thread sleeps until the phase completes or this hint elapses,
+// instead of spinning and taking issue slots from working warps.
+constexpr uint32_t kTryWaitSuspendNs = 20000u;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kTryWaitSuspendNs)
+        : "memory");
+    return ok != 0u;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase of parity `parity` to complete, giving up after
+// kWaitTimeoutNs (returns false; the caller flags the failure and stops).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+    }
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Bulk copy global -> shared (16-byte aligned, size a multiple of 16),
+// completion counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // ---------------------------------------------------------------- epilogue math
 
 // Angle of pair index d at position pos: the f32 product pos * inv_freq[d].
@@ -90,9 +171,11 @@ __device__ __forceinline__ void kv_put(void* kv, int f16, size_t idx, float v) {
 __device__ __forceinline__ bool pos_ok(int pos, int n_ctx) { return pos >= 0 && pos < n_ctx; }
 
 __device__ __forceinline__ void flag_bad_pos(int pos) {
-    atomicOr(&g_qkv_status[0], 1u);
+    atomicOr(&g_qkv_status[0], kFlagPosRange);
     atomicExch(&g_qkv_status[1], static_cast<unsigned int>(pos));
 }
+
+__device__ __forceinline__ void flag_timeout() { atomicOr(&g_qkv_status[0], kFlagTimeout); }
 
 // q (sec 0) or k (sec 1) pair: bias, rotate, write back; k also goes to the cache.
 __device__ __forceinline__ void epi_qk_pair(const DecodeParams& p, int sec, int j, int j2, float y0,
@@ -307,6 +390,277 @@ __global__ void __launch_bounds__(256) qkv_decode_kernel(const __grid_constant__
     }
 }
 
+// ---------------------------------------------------------------- bulk-copy pipelined projection
+
+// Persistent variant for 16-byte aligned rows: one CTA per SM owns a
+// contiguous range of row-pair units.  A producer warp streams each unit's two
+// rows (2 x H weights) into a ring of shared-memory stages with cp.async.bulk
+// (L2 evict-first: each byte is used once), ahead of the consumers.  Consumer
+// group g (G warps) owns stages g, g + NG, ... and reduces whole units from
+// shared memory: with a stage count that is a multiple of the group count NG,
+// unit i and unit i - S (the previous user of its stage) belong to the same
+// group, so every group waits on each stage's phases strictly in order and a
+// parity wait can never alias a phase two rounds ahead.  The G warps of a
+// group split the 16-byte chunks of the unit's rows (thread t of the group
+// takes chunks t, t + 32G, ...) and combine their partials in warp order
+// through shared memory under a group-wide named barrier.  The producer starts before griddepcontrol.wait:
+// weights are never written by the preceding grid, so under programmatic
+// dependent launch a layer's weight stream starts while the previous layer
+// finishes.
+//
+// Per row the sum is: group thread t takes chunks t, t + 32G, ... in
+// increasing order, accumulating even and odd elements in the two halves of
+// packed f32x2 FMAs; the halves are added, a xor butterfly sums each warp,
+// then the G warp partials are added in warp order.  The order depends only
+// on H and G, not on the layer class, so concat and mixed layers give
+// identical bits.
+#ifndef QKV_DECODE_GROUPS
+#define QKV_DECODE_GROUPS 4
+#endif
+#ifndef QKV_DECODE_GROUP_WARPS
+#define QKV_DECODE_GROUP_WARPS 2
+#endif
+constexpr int kGroups = QKV_DECODE_GROUPS;            // NG: consumer groups (stage owners)
+constexpr int kGroupWarps = QKV_DECODE_GROUP_WARPS;   // G: warps per group
+constexpr int kConsumerWarps = kGroups * kGroupWarps;
+constexpr int kTmaThreads = (kConsumerWarps + 1) * 32;
+
+#ifndef QKV_DECODE_PAIRS
+#define QKV_DECODE_PAIRS 1
+#endif
+constexpr int kPairs = QKV_DECODE_PAIRS;  // P: neox pairs per unit (rows per bulk copy)
+
+// Unit u of the ring kernel: up to P consecutive neox pairs (d0 .. d0+n-1) of
+// one q or k head — two contiguous blocks of n rows, (h*hd + d0 ...) and
+// (h*hd + hd/2 + d0 ...) — or 2n consecutive v rows (blocks r.. and r+n..).
+struct Unit {
+    int sec;  // 0 q, 1 k, 2 v
+    int r;    // first row of block A (section-local)
+    int n;    // rows per block
+    int off;  // block B starts at row r + off
+};
+
+__device__ __forceinline__ Unit unit_info(int u, int nqt, int nkt, int hd) {
+    const int half = hd >> 1;
+    const int per_head = (half + kPairs - 1) / kPairs;
+    const int uq = (nqt / hd) * per_head, uk = (nkt / hd) * per_head;
+    Unit t;
+    if (u < uq + uk) {
+        t.sec = (u < uq) ? 0 : 1;
+        const int v = t.sec ? u - uq : u;
+        const int h = v / per_head;
+        const int d0 = (v - h * per_head) * kPairs;
+        t.n = min(kPairs, half - d0);
+        t.r = h * hd + d0;
+        t.off = half;
+    } else {
+        t.sec = 2;
+        t.r = (u - uq - uk) * 2 * kPairs;
+        t.n = min(kPairs, (nkt - t.r) >> 1);
+        t.off = t.n;
+    }
+    return t;
+}
+
+__host__ __device__ __forceinline__ int unit_count(int nqt, int nkt, int hd) {
+    const int per_head = ((hd >> 1) + kPairs - 1) / kPairs;
+    return (nqt / hd) * per_head + (nkt / hd) * per_head + (nkt + 2 * kPairs - 1) / (2 * kPairs);
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(smem_u32(p)));
+    return r;
+}
+
+__device__ __forceinline__ float4 ld_shared_f4(const void* p) {
+    float4 r;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+                 : "r"(smem_u32(p)));
+    return r;
+}
+
+__device__ __forceinline__ float2 bf16x2_to_f32x2(uint32_t u) {
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+}
+
+// acc += 16-byte weight chunk * its x slice (bf16: 8 values in xa, xb; f32: 4
+// values in xa), even elements in acc.x, odd in acc.y.
+template <typename WT>
+__device__ __forceinline__ float2 fma2_chunk(uint4 w, float4 xa, float4 xb, float2 acc) {
+    if constexpr (sizeof(WT) == 2) {
+        acc = __ffma2_rn(bf16x2_to_f32x2(w.x), make_float2(xa.x, xa.y), acc);
+        acc = __ffma2_rn(bf16x2_to_f32x2(w.y), make_float2(xa.z, xa.w), acc);
+        acc = __ffma2_rn(bf16x2_to_f32x2(w.z), make_float2(xb.x, xb.y), acc);
+        acc = __ffma2_rn(bf16x2_to_f32x2(w.w), make_float2(xb.z, xb.w), acc);
+    } else {
+        acc = __ffma2_rn(make_float2(__uint_as_float(w.x), __uint_as_float(w.y)), make_float2(xa.x, xa.y), acc);
+        acc = __ffma2_rn(make_float2(__uint_as_float(w.z), __uint_as_float(w.w)), make_float2(xa.z, xa.w), acc);
+    }
+    return acc;
+}
+
+// Both rows of a unit, staged: group thread t takes chunks t, t + 32G, ...; x
+// is staged as float4 planes (bf16: x[8c..8c+3] and x[8c+4..8c+7]; f32:
+// x[4c..4c+3]).  Returns the warp's partial of each row (same in every lane).
+template <typename WT>
+__device__ __forceinline__ void dot2_staged(const unsigned char* row0, const unsigned char* row1,
+                                            const float4* xs, int H, int t, float& a0, float& a1) {
+    constexpr bool kBf16 = sizeof(WT) == 2;
+    const int nch = H / (kBf16 ? 8 : 4);
+    const float4* xb = xs + nch;
+    float2 c0 = make_float2(0.f, 0.f), c1 = make_float2(0.f, 0.f);
+#pragma unroll 4
+    for (int c = t; c < nch; c += 32 * kGroupWarps) {
+        const uint4 v0 = ld_shared_v4(row0 + 16 * c);
+        const uint4 v1 = ld_shared_v4(row1 + 16 * c);
+        const float4 xa = ld_shared_f4(xs + c);
+        const float4 x2 = kBf16 ? ld_shared_f4(xb + c) : xa;
+        c0 = fma2_chunk<WT>(v0, xa, x2, c0);
+        c1 = fma2_chunk<WT>(v1, xa, x2, c1);
+    }
+    a0 = warp_sum(__fadd_rn(c0.x, c0.y));
+    a1 = warp_sum(__fadd_rn(c1.x, c1.y));
+}
+
+template <typename WT, int MODE>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+    qkv_decode_tma_kernel(const __grid_constant__ DecodeParams p, int stages, uint32_t stage_bytes,
+                          uint32_t x_bytes) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ float freq_s[QKV_MAX_HEAD_DIM / 2];
+    __shared__ float gpart[kGroups][kGroupWarps][2];
+    float4* xs4 = reinterpret_cast<float4*>(smem);
+    unsigned char* ring = smem + x_bytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + static_cast<size_t>(stages) * stage_bytes);
+    uint64_t* empty = full + stages;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int half = p.hd >> 1;
+    const int units = unit_count(p.nqt, p.nkt, p.hd);
+    const int u_begin = static_cast<int>(static_cast<long long>(units) * blockIdx.x / gridDim.x);
+    const int u_end = static_cast<int>(static_cast<long long>(units) * (blockIdx.x + 1) / gridDim.x);
+    const int n = u_end - u_begin;
+    const uint32_t row_bytes = static_cast<uint32_t>(p.H) * sizeof(WT);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+    // The next layer's grid may be scheduled now: it reads and writes nothing of
+    // ours before its own griddepcontrol.wait, which waits for this grid to finish.
+    griddep_launch_dependents();
+
+    if (warp == kConsumerWarps) {
+        // ---- producer: one lane issues all bulk copies of this CTA ----
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_first();
+            int issued = 0;
+            for (int i = 0; i < n; ++i) {
+                const int s = i % stages;
+                if (i >= stages && !mbar_wait_bounded(&empty[s], ((i / stages) - 1) & 1)) {
+                    flag_timeout();
+                    break;
+                }
+                const Unit t = unit_info(u_begin + i, p.nqt, p.nkt, p.hd);
+                const unsigned char* w = static_cast<const unsigned char*>(p.w[t.sec]);
+                unsigned char* dst = ring + static_cast<size_t>(s) * stage_bytes;
+                const uint32_t blk = static_cast<uint32_t>(t.n) * row_bytes;
+                mbar_arrive_expect_tx(&full[s], 2 * blk);
+                bulk_g2s(dst, w + static_cast<size_t>(t.r) * row_bytes, blk, &full[s], pol);
+                bulk_g2s(dst + blk, w + static_cast<size_t>(t.r + t.off) * row_bytes, blk, &full[s], pol);
+                ++issued;
+            }
+            // Drain: no copy may still be landing in shared memory when the CTA exits.
+            const int first = issued > stages ? issued - stages : 0;
+            for (int i = first; i < issued; ++i)
+                if (!mbar_wait_bounded(&full[i % stages], (i / stages) & 1)) flag_timeout();
+        }
+        return;
+    }
+
+    // ---- consumers ----
+    griddep_wait();
+    {
+        const int H = p.H;
+        const int tid = threadIdx.x, nthr = kConsumerWarps * 32;
+        if constexpr (sizeof(WT) == 2) {
+            const int nch = H / 8;
+            const float4* xg = reinterpret_cast<const float4*>(p.x);
+            for (int c = tid; c < nch; c += nthr) {
+                xs4[c] = xg[2 * c];
+                xs4[nch + c] = xg[2 * c + 1];
+            }
+        } else {
+            const float4* xg = reinterpret_cast<const float4*>(p.x);
+            for (int c = tid; c < H / 4; c += nthr) xs4[c] = xg[c];
+        }
+        for (int i = tid; i < half; i += nthr) freq_s[i] = p.inv_freq[i];
+    }
+    named_barrier_sync(1, kConsumerWarps * 32);
+    const int pos = (MODE == kFused) ? *p.pos : 0;
+    const bool store = pos_ok(pos, p.n_ctx);
+    if (MODE == kFused && !store && blockIdx.x == 0 && threadIdx.x == 0) flag_bad_pos(pos);
+
+    const int group = warp / kGroupWarps, gw = warp % kGroupWarps;
+    const int gt = gw * 32 + lane;  // thread index within the group
+    for (int i = group; i < n; i += kGroups) {
+        const int s = i % stages;
+        if (!mbar_wait_bounded(&full[s], (i / stages) & 1)) {
+            if (lane == 0) flag_timeout();
+            break;
+        }
+        const Unit t = unit_info(u_begin + i, p.nqt, p.nkt, p.hd);
+        const unsigned char* st = ring + static_cast<size_t>(s) * stage_bytes;
+        const uint32_t blk = static_cast<uint32_t>(t.n) * row_bytes;
+        for (int j = 0; j < t.n; ++j) {
+            float a0, a1;
+            dot2_staged<WT>(st + j * row_bytes, st + blk + j * row_bytes, xs4, p.H, gt, a0, a1);
+            const bool last = (j == t.n - 1);
+            if constexpr (kGroupWarps > 1) {
+                if (lane == 0) {
+                    gpart[group][gw][0] = a0;
+                    gpart[group][gw][1] = a1;
+                }
+                // the group's reads of this pair are done and its partials published
+                named_barrier_sync(2 + group, 32 * kGroupWarps);
+                if (gw == 0) {
+                    a0 = gpart[group][0][0];
+                    a1 = gpart[group][0][1];
+                    for (int w = 1; w < kGroupWarps; ++w) {
+                        a0 = __fadd_rn(a0, gpart[group][w][0]);
+                        a1 = __fadd_rn(a1, gpart[group][w][1]);
+                    }
+                }
+                // keep the partial slots until warp 0 of the group has read them
+                named_barrier_sync(2 + kGroups + group, 32 * kGroupWarps);
+            } else {
+                __syncwarp();
+            }
+            if (last && gw == 0 && lane == 0) mbar_arrive(&empty[s]);
+            if (gw == 0 && lane == 0) {
+                const int r0 = t.r + j, r1 = t.r + t.off + j;
+                if constexpr (MODE == kProjectOnly) {
+                    p.out[t.sec][r0] = a0;
+                    p.out[t.sec][r1] = a1;
+                } else if (t.sec < 2) {
+                    epi_qk_pair(p, t.sec, r0, r1, a0, a1, pos, freq_s[r0 % p.hd], store);
+                } else {
+                    epi_v_elem(p, r0, a0, pos, store);
+                    epi_v_elem(p, r1, a1, pos, store);
+                }
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------- standalone epilogue
 
 // One thread per unit of the flat index: q pairs, then k pairs, then v elements.
@@ -384,8 +738,72 @@ cudaError_t launch_ex(K kernel, dim3 grid, dim3 block, size_t smem, bool pdl, cu
     return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
+int sm_count() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+    }
+    return n;
+}
+
+// Dynamic shared memory per CTA: the ring takes what one CTA per SM can have,
+// which keeps the most weight bytes in flight.
+#ifndef QKV_DECODE_SMEM_KB
+#define QKV_DECODE_SMEM_KB 225
+#endif
+// Dynamic shared memory per CTA for x plus the ring (one CTA per SM).
+constexpr size_t kSmemBudget = QKV_DECODE_SMEM_KB * 1024;
+constexpr int kMaxStages = 32;
+
+// Stages of the ring for this shape (a multiple of the consumer count), or 0
+// when the shape needs the register-streaming kernel (unaligned rows, or rows
+// too long to stage).
+template <typename WT>
+int tma_stages(const DecodeParams& p, uint32_t& stage_bytes, uint32_t& x_bytes) {
+    const size_t row = static_cast<size_t>(p.H) * sizeof(WT);
+    stage_bytes = static_cast<uint32_t>((2 * kPairs * row + 127) / 128 * 128);
+    x_bytes = static_cast<uint32_t>((static_cast<size_t>(p.H) * 4 + 127) / 128 * 128);
+    const size_t barriers = 2 * kMaxStages * sizeof(uint64_t);
+    if (x_bytes + barriers + static_cast<size_t>(kGroups) * stage_bytes > kSmemBudget) return 0;
+    int st = static_cast<int>((kSmemBudget - x_bytes - barriers) / stage_bytes);
+    st = st > kMaxStages ? kMaxStages : st;
+    st -= st % kGroups;
+    return st;
+}
+
+template <typename WT, int MODE>
+cudaError_t launch_decode_tma(const DecodeParams& p, int stages, uint32_t stage_bytes, uint32_t x_bytes,
+                              bool pdl, cudaStream_t stream) {
+    auto kernel = qkv_decode_tma_kernel<WT, MODE>;
+    const size_t smem = x_bytes + static_cast<size_t>(stages) * stage_bytes + 2 * stages * sizeof(uint64_t);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const int units = unit_count(p.nqt, p.nkt, p.hd);
+    const int grid = units < sm_count() ? units : sm_count();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kTmaThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, p, stages, stage_bytes, x_bytes);
+}
+
 template <typename WT, bool VEC, int MODE>
 cudaError_t launch_decode_t(const DecodeParams& p, bool pdl, cudaStream_t stream) {
+    if constexpr (VEC) {
+        uint32_t stage_bytes = 0, x_bytes = 0;
+        const int st = tma_stages<WT>(p, stage_bytes, x_bytes);
+        if (st > 0) return launch_decode_tma<WT, MODE>(p, st, stage_bytes, x_bytes, pdl, stream);
+    }
     auto kernel = qkv_decode_kernel<WT, VEC, MODE>;
     const size_t smem = static_cast<size_t>(p.H) * sizeof(float);
     if (smem > 48 * 1024) {

@@ -80,6 +80,8 @@ SHAPES = [
     (896, 14, 2, 64, "f32", "f32", 512, 17),   # Qwen2.5-0.5B single layer
     (3584, 28, 4, 128, "bf16", "f16", 4096, 1641),  # Qwen2.5-7B layer
     (5120, 40, 8, 128, "bf16", "f16", 4096, 3254),  # Qwen2.5-14B layer
+    (256, 64, 8, 128, "bf16", "f16", 64, 33),  # 5120 row pairs, 16-stage ring wraps twice per CTA
+    (1024, 96, 16, 64, "f32", "f32", 40, 39),  # f32 rows, 4 KB stages, ring wraps per CTA
 ]
 
 
