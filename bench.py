@@ -215,13 +215,8 @@ def barrier_sync(world):
 
 
 def max_over_ranks(v: float, world: int) -> float:
-    if world == 1:
-        return v
-    import torch
-    import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    from qkv_rope_kv_gb300 import shard
+    return v if world == 1 else shard.max_over_ranks(v, device="cuda")
 
 
 # ---------------------------------------------------------------- CPU baseline (oracle)
