@@ -28,9 +28,13 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "epilogue_math.cuh"
+#include "ptx_sync.cuh"
 #include "qkv_internal.h"
 
 namespace {
+using namespace qkv_epi;
+using namespace qkv_ptx;
 
 constexpr int kUnroll = 4;  // 16-byte loads in flight per lane per row
 
@@ -38,14 +42,6 @@ constexpr int kUnroll = 4;  // 16-byte loads in flight per lane per row
 __device__ unsigned int g_qkv_status[2];
 
 // ---------------------------------------------------------------- PTX helpers
-
-// Programmatic dependent launch.  Without the launch attribute both are no-ops.
-__device__ __forceinline__ void griddep_wait() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-__device__ __forceinline__ void griddep_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
 
 // 16-byte weight load: read-only for the kernel's lifetime, streamed once,
 // so it bypasses L1 allocation.
@@ -66,109 +62,12 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// ---------------------------------------------------------------- mbarrier / bulk copy
+// ---------------------------------------------------------------- status flags
 
-constexpr uint64_t kWaitTimeoutNs = 500ull * 1000ull * 1000ull;  // 0.5 s: far beyond any healthy wait
 constexpr unsigned int kFlagPosRange = 1u;
 constexpr unsigned int kFlagTimeout = 2u;
-// A waiting thread sleeps until the phase completes or this hint elapses,
-// instead of spinning and taking issue slots from working warps.
-constexpr uint32_t kTryWaitSuspendNs = 20000u;
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_fence_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(kTryWaitSuspendNs)
-        : "memory");
-    return ok != 0u;
-}
-
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Wait for the phase of parity `parity` to complete, giving up after
-// kWaitTimeoutNs (returns false; the caller flags the failure and stops).
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (;;) {
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
-    }
-}
-
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-
-// Bulk copy global -> shared (16-byte aligned, size a multiple of 16),
-// completion counted in bytes on `bar`.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                         uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
-        "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
 // ---------------------------------------------------------------- epilogue math
-
-// Angle of pair index d at position pos: the f32 product pos * inv_freq[d].
-__device__ __forceinline__ float rope_theta(int pos, float inv_freq) {
-    return __fmul_rn(__int2float_rn(pos), inv_freq);
-}
-
-// Neox rotation of the pair (x0, x1) = (element d, element d + hd/2).
-__device__ __forceinline__ void rope_rotate(float x0, float x1, float theta, float& r0, float& r1) {
-    float s, c;
-    sincosf(theta, &s, &c);
-    r0 = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, s));
-    r1 = __fadd_rn(__fmul_rn(x0, s), __fmul_rn(x1, c));
-}
-
-// Cache element store at flat index pos * nkt + j (f32, or f16 round-to-nearest-even).
-__device__ __forceinline__ void kv_put(void* kv, int f16, size_t idx, float v) {
-    if (f16) reinterpret_cast<__half*>(kv)[idx] = __float2half_rn(v);
-    else reinterpret_cast<float*>(kv)[idx] = v;
-}
-
-__device__ __forceinline__ bool pos_ok(int pos, int n_ctx) { return pos >= 0 && pos < n_ctx; }
+// rope_theta, rope_rotate, kv_put, pos_ok: epilogue_math.cuh (shared with prefill).
 
 __device__ __forceinline__ void flag_bad_pos(int pos) {
     atomicOr(&g_qkv_status[0], kFlagPosRange);

@@ -1,7 +1,393 @@
-// Prefill (nt >= 1) for the concat class: tcgen05 bf16 GEMM + per-token epilogue.
+// Prefill (nt >= 1 tokens) of the attention-input stage on sm_103a: the dense
+// contraction Y = X W^T on the 5th-generation tensor cores, with the per-token
+// epilogue (bias, neox RoPE at positions[t], KV-cache store) applied to the
+// accumulator as it leaves tensor memory.
+//
+// The page keeps prefill on the unfused chain (its fused epilogue is gated to
+// nt == 1: "73 · D3-8 — G4 FusedQKV ported to CUDA", §3.2 Excerpt D and §3.3);
+// the per-token math is the decode math of §3.2 Excerpt A at pos = positions[t],
+// computed by the same device functions (epilogue_math.cuh).
+//
+// Tiling.  One CTA computes a tile of 128 tokens (UMMA M) x 64 weight rows
+// (UMMA N).  The 64 rows are two 32-row boxes chosen so that every neox pair
+// lands in one thread: for a q or k tile, rows (h*hd + d0 .. +31) and
+// (h*hd + hd/2 + d0 .. +31); for a v tile, 64 consecutive rows.  K advances in
+// blocks of 64 bf16 (128 bytes, one 128B-swizzle row).  Warp 0 lane 0 loads
+// X and W tiles with TMA into a 6-stage ring (mbarrier transaction counts);
+// warp 1 lane 0 issues tcgen05.mma (kind::f16, bf16 x bf16 -> f32 in TMEM,
+// 4 MMAs of K = 16 per stage) and frees each stage with tcgen05.commit; then
+// all four warps read their 32 TMEM lanes (one token each) with tcgen05.ld and
+// run the epilogue.  Every wait is bounded; on expiry the kernel flags the
+// device status word, drains in-flight copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+#include "epilogue_math.cuh"
+#include "ptx_sync.cuh"
 #include "qkv_internal.h"
 
-qkv_status launch_prefill(const PrefillParams&, cudaStream_t, const char** why) {
-    *why = "the tcgen05 prefill kernel is not built into this library yet";
-    return QKV_ERR_UNSUPPORTED;
+namespace {
+using namespace qkv_epi;
+using namespace qkv_ptx;
+
+constexpr int kBM = 128;                       // tokens per tile (UMMA M)
+constexpr int kBN = 64;                        // weight rows per tile (UMMA N)
+constexpr int kBox = 32;                       // rows per W box
+constexpr int kBK = 64;                        // K per stage (bf16): 128 bytes
+constexpr int kUK = 16;                        // K per tcgen05.mma, kind::f16
+constexpr int kStages = 6;
+constexpr int kThreads = 128;
+constexpr uint32_t kABytes = kBM * kBK * 2;    // 16 KB
+constexpr uint32_t kBBytes = kBN * kBK * 2;    // 8 KB
+constexpr uint32_t kBoxBytes = kBox * kBK * 2; // 4 KB
+constexpr uint32_t kTmemCols = 64;             // f32 accumulator columns (= kBN)
+constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStages * (kABytes + kBBytes) +
+                              (2 * kStages + 1) * sizeof(uint64_t) + 16;
+
+constexpr unsigned int kFlagPosRange = 1u;
+constexpr unsigned int kFlagTimeout = 2u;
+
+// Device status word of the prefill kernels: [0] flags, [1] a bad position.
+__device__ unsigned int g_prefill_status[2];
+
+__device__ __forceinline__ void flag_bad_pos(int pos) {
+    atomicOr(&g_prefill_status[0], kFlagPosRange);
+    atomicExch(&g_prefill_status[1], static_cast<unsigned int>(pos));
+}
+__device__ __forceinline__ void flag_timeout() { atomicOr(&g_prefill_status[0], kFlagTimeout); }
+
+// ---------------------------------------------------------------- TMA
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---------------------------------------------------------------- tcgen05
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile written by TMA with the
+// 128-byte swizzle: rows of 128 bytes, 8-row (1024-byte) swizzle atoms stacked
+// along M/N (stride-dimension byte offset 1024), descriptor version 1,
+// layout type SWIZZLE_128B (2).  The leading-dimension offset is unused for
+// swizzled K-major operands and set to 1 (16 bytes).
+__device__ __forceinline__ uint64_t smem_desc_k128(const void* tile) {
+    const uint64_t addr = smem_u32(tile);
+    uint64_t d = 0;
+    d |= (addr & 0x3FFFFull) >> 4;        // bits 0-13: start address >> 4
+    d |= 1ull << 16;                      // bits 16-29: leading byte offset >> 4
+    d |= (1024ull >> 4) << 32;            // bits 32-45: stride byte offset >> 4
+    d |= 1ull << 46;                      // bits 46-48: fixed 0b001
+    d |= 2ull << 61;                      // bits 61-63: 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major, N = 64, M = 128.
+constexpr uint32_t kIdesc = (1u << 4)             // D format: f32
+                            | (1u << 7)           // A format: bf16
+                            | (1u << 10)          // B format: bf16
+                            | ((kBN >> 3) << 17)  // N >> 3
+                            | ((kBM >> 4) << 24); // M >> 4
+
+__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(da), "l"(db), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+// 32 consecutive f32 columns of this warp's 32 TMEM lanes: thread l gets lane
+// (warp's base lane + l), columns col .. col + 31.
+__device__ __forceinline__ void tc_ld_32cols(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------- kernel
+
+__global__ void __launch_bounds__(kThreads, 1)
+    qkv_prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                       const __grid_constant__ PrefillParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    __shared__ float bias_s[kBN];
+    __shared__ float freq_s[kBox];
+    __shared__ uint32_t tmem_slot;
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    unsigned char* sA = smem;
+    unsigned char* sB = smem + kStages * kABytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
+    uint64_t* empty = full + kStages;
+    uint64_t* done = empty + kStages;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.y * kBM;
+    const int half = p.hd >> 1;
+    const int tiles_per_head = p.hd / kBN;
+    const int tq = p.nqt / kBN, tk = p.nkt / kBN;
+    const int tile = blockIdx.x;
+    int sec, rowA, rowB, d0;  // section and section-local first rows of the two boxes
+    if (tile < tq + tk) {
+        sec = tile < tq ? 0 : 1;
+        const int v = sec ? tile - tq : tile;
+        const int h = v / tiles_per_head;
+        d0 = (v - h * tiles_per_head) * kBox;
+        rowA = h * p.hd + d0;
+        rowB = rowA + half;
+    } else {
+        sec = 2;
+        d0 = 0;
+        rowA = (tile - tq - tk) * kBN;
+        rowB = rowA + kBox;
+    }
+    const int base = sec == 0 ? 0 : (sec == 1 ? p.nqt : p.nqt + p.nkt);  // section's first global row
+    const int nk = (p.H + kBK - 1) / kBK;
+
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (threadIdx.x == 32) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(done, 1);
+        mbar_fence_init();
+    }
+    if (threadIdx.x < kBox) bias_s[threadIdx.x] = p.bias[base + rowA + threadIdx.x];
+    else if (threadIdx.x < 2 * kBox) bias_s[threadIdx.x] = p.bias[base + rowB + threadIdx.x - kBox];
+    else if (threadIdx.x < 3 * kBox && sec < 2) freq_s[threadIdx.x - 2 * kBox] = p.inv_freq[d0 + threadIdx.x - 2 * kBox];
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ---- producer: TMA tiles of X (128 x 64) and W (two 32 x 64 boxes) per stage ----
+        prefetch_tensormap(&tm_x);
+        prefetch_tensormap(&tm_w);
+        int issued = 0;
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % kStages;
+            if (kb >= kStages && !mbar_wait_bounded(&empty[s], ((kb / kStages) - 1) & 1)) {
+                flag_timeout();
+                break;
+            }
+            mbar_arrive_expect_tx(&full[s], kABytes + kBBytes);
+            tma_load_2d(sA + s * kABytes, &tm_x, kb * kBK, m0, &full[s]);
+            tma_load_2d(sB + s * kBBytes, &tm_w, kb * kBK, base + rowA, &full[s]);
+            tma_load_2d(sB + s * kBBytes + kBoxBytes, &tm_w, kb * kBK, base + rowB, &full[s]);
+            ++issued;
+        }
+        // Drain: no copy may still be landing in shared memory when the CTA exits.
+        const int first = issued > kStages ? issued - kStages : 0;
+        for (int kb = first; kb < issued; ++kb)
+            if (!mbar_wait_bounded(&full[kb % kStages], (kb / kStages) & 1)) flag_timeout();
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer ----
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % kStages;
+            if (!mbar_wait_bounded(&full[s], (kb / kStages) & 1)) {
+                flag_timeout();
+                break;
+            }
+            tc_fence_after();
+            const unsigned char* a = sA + s * kABytes;
+            const unsigned char* b = sB + s * kBBytes;
+#pragma unroll
+            for (int k = 0; k < kBK / kUK; ++k)
+                tc_mma(tmem, smem_desc_k128(a + k * kUK * 2), smem_desc_k128(b + k * kUK * 2), (kb | k) != 0);
+            tc_commit(&empty[s]);  // the stage is free once these MMAs have read it
+        }
+        tc_commit(done);  // arrives when every MMA issued above has completed
+    }
+    __syncwarp();
+
+    // ---- epilogue: thread (warp, lane) owns TMEM lane 32*warp + lane = token m0 + that ----
+    // Warp-uniform: tcgen05.ld below is a warp-collective instruction.
+    const bool acc_ready = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(done, 0));
+    if (!acc_ready && lane == 0) flag_timeout();
+    tc_fence_after();
+    float acc[kBN];
+    if (acc_ready) {
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        tc_ld_32cols(taddr, acc);
+        tc_ld_32cols(taddr + kBox, acc + kBox);
+        tc_wait_ld();
+    }
+    const int t = m0 + warp * 32 + lane;
+    if (acc_ready && t < p.nt) {
+        const int pos = p.positions[t];
+        const bool store = pos_ok(pos, p.n_ctx);
+        if (!store) flag_bad_pos(pos);
+        const int R = p.nqt + 2 * p.nkt;
+        float* yrow = p.Y + static_cast<size_t>(t) * R + base;
+        const size_t kvrow = static_cast<size_t>(store ? pos : 0) * static_cast<size_t>(p.nkt);
+        if (sec < 2) {
+#pragma unroll
+            for (int i = 0; i < kBox; ++i) {
+                const float x0 = __fadd_rn(acc[i], bias_s[i]);
+                const float x1 = __fadd_rn(acc[kBox + i], bias_s[kBox + i]);
+                float r0, r1;
+                rope_rotate(x0, x1, rope_theta(pos, freq_s[i]), r0, r1);
+                acc[i] = r0;
+                acc[kBox + i] = r1;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < kBN; ++i) acc[i] = __fadd_rn(acc[i], bias_s[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < kBox; i += 4) {
+            *reinterpret_cast<float4*>(yrow + rowA + i) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+            *reinterpret_cast<float4*>(yrow + rowB + i) =
+                make_float4(acc[kBox + i], acc[kBox + i + 1], acc[kBox + i + 2], acc[kBox + i + 3]);
+        }
+        if (store && sec > 0) {
+            void* kv = sec == 1 ? p.kv_k : p.kv_v;
+#pragma unroll
+            for (int i = 0; i < kBox; ++i) {
+                kv_put(kv, p.kv_f16, kvrow + rowA + i, acc[i]);
+                kv_put(kv, p.kv_f16, kvrow + rowB + i, acc[kBox + i]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        // After a timeout, give in-flight MMAs a second bounded wait before the
+        // accumulator columns are released.
+        if (!acc_ready) mbar_wait_bounded(done, 0);
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows x cols] matrix, box [box_rows x 64],
+// 128-byte swizzle, out-of-bounds elements read as zero.
+bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+qkv_status launch_prefill(const PrefillParams& p, cudaStream_t stream, const char** why) {
+    if (p.hd % kBN != 0) {
+        *why = "head_dim must be a multiple of 64 (two 32-row boxes per neox tile)";
+        return QKV_ERR_UNSUPPORTED;
+    }
+    if (p.H % 8 != 0) {
+        *why = "hidden must be a multiple of 8 (16-byte TMA row stride)";
+        return QKV_ERR_UNSUPPORTED;
+    }
+    if ((reinterpret_cast<uintptr_t>(p.X) | reinterpret_cast<uintptr_t>(p.W)) & 15) {
+        *why = "X and W must be 16-byte aligned";
+        return QKV_ERR_INVALID_ARG;
+    }
+    if (reinterpret_cast<uintptr_t>(p.Y) & 15) {
+        *why = "Y must be 16-byte aligned";
+        return QKV_ERR_INVALID_ARG;
+    }
+    const int R = p.nqt + 2 * p.nkt;
+    CUtensorMap tm_x, tm_w;
+    if (!encode_bf16_2d(&tm_x, p.X, static_cast<uint64_t>(p.nt), static_cast<uint64_t>(p.H), kBM) ||
+        !encode_bf16_2d(&tm_w, p.W, static_cast<uint64_t>(R), static_cast<uint64_t>(p.H), kBox)) {
+        *why = "cuTensorMapEncodeTiled failed or is unavailable";
+        return QKV_ERR_CUDA;
+    }
+    cudaError_t e = cudaFuncSetAttribute(qkv_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) {
+        *why = cudaGetErrorString(e);
+        return QKV_ERR_CUDA;
+    }
+    const dim3 grid(R / kBN, (p.nt + kBM - 1) / kBM);
+    qkv_prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_x, tm_w, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        *why = cudaGetErrorString(e);
+        return QKV_ERR_CUDA;
+    }
+    return QKV_OK;
+}
+
+cudaError_t prefill_status_read(cudaStream_t stream, uint32_t* flags, int32_t* bad_pos) {
+    unsigned int h[2] = {0u, 0u};
+    cudaError_t e = cudaMemcpyFromSymbolAsync(h, g_prefill_status, sizeof(h), 0, cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return e;
+    if (h[0] != 0u) {
+        const unsigned int zero[2] = {0u, 0u};
+        e = cudaMemcpyToSymbolAsync(g_prefill_status, zero, sizeof(zero), 0, cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess) return e;
+        e = cudaStreamSynchronize(stream);
+        if (e != cudaSuccess) return e;
+    }
+    *flags = h[0];
+    *bad_pos = static_cast<int32_t>(h[1]);
+    return cudaSuccess;
 }

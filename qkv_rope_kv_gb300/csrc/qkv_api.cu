@@ -507,10 +507,14 @@ extern "C" void qkv_model_graph_destroy(qkv_graph* g) {
 // ------------------------------------------------------------------ device status
 
 extern "C" qkv_status qkv_check_device_error(void* stream, uint32_t* flags_out, int32_t* bad_pos_out) {
-    uint32_t flags = 0;
-    int32_t bad = 0;
+    uint32_t flags = 0, pflags = 0;
+    int32_t bad = 0, pbad = 0;
     cudaError_t e = device_status_read(static_cast<cudaStream_t>(stream), &flags, &bad);
     if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+    e = prefill_status_read(static_cast<cudaStream_t>(stream), &pflags, &pbad);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the prefill status word");
+    if (!flags) bad = pbad;
+    flags |= pflags;
     if (flags_out) *flags_out = flags;
     if (bad_pos_out) *bad_pos_out = bad;
     if (flags) return fail(QKV_ERR_DEVICE_FLAG, "device status flags 0x%x (position %d outside [0, n_ctx))",

@@ -53,3 +53,4 @@ struct PrefillParams {
     float inv_freq[QKV_MAX_HEAD_DIM / 2];
 };
 qkv_status launch_prefill(const PrefillParams& p, cudaStream_t stream, const char** why);
+cudaError_t prefill_status_read(cudaStream_t stream, uint32_t* flags, int32_t* bad_pos);
