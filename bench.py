@@ -380,6 +380,86 @@ def native_arm(args, w):
         dist.destroy_process_group()
 
 
+def prefill_algo(w: configs.Workload):
+    """Bytes and flops one prefill layer must move/do: W, X, bias read; Y and nt cache rows written."""
+    bytes_ = (w.w_bytes() + w.nt * w.hidden * 2 + 4 * w.rows + 4 * w.nt * w.rows
+              + 2 * w.nt * w.nkt * w.kv_elem_bytes())
+    flops = 2 * w.nt * w.rows * w.hidden
+    return bytes_, flops
+
+
+def prefill_arm(args, w):
+    import torch
+    import qkv_rope_kv_gb300 as Q
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    Q.load()
+    seed = rank
+    plan = Q.qkv_plan_create(w.hidden, w.n_head, w.n_head_kv, w.head_dim, w.theta, w.n_ctx,
+                             w_dtype=Q.QKV_BF16, kv_dtype=Q.QKV_F16 if w.kv_dtype == "f16" else Q.QKV_F32,
+                             freq_scale=w.freq_scale)
+    positions = torch.arange(w.nt, dtype=torch.int32, device="cuda")
+    kvt = torch.int16 if w.kv_dtype == "f16" else torch.float32
+    layers = []
+    hostW = np.empty((w.rows, w.hidden), np.uint16)
+    for l in range(w.n_layers):
+        synth.weight_rows(seed, l, 0, w.rows, w.hidden, "bf16", out=hostW)
+        layers.append(dict(
+            X=torch.from_numpy(synth.prefill_x(seed, l, w.nt, w.hidden).view(np.int16)).to("cuda"),
+            w=torch.from_numpy(hostW.view(np.int16)).to("cuda"),
+            bias=torch.from_numpy(synth.bias(seed, l, w.rows)).to("cuda"),
+            positions=positions,
+            Y=torch.empty(w.nt, w.rows, dtype=torch.float32, device="cuda"),
+            kv_k=torch.zeros(w.n_ctx, w.nkt, dtype=kvt, device="cuda"),
+            kv_v=torch.zeros(w.n_ctx, w.nkt, dtype=kvt, device="cuda")))
+    stream = torch.cuda.Stream()
+    graph = Q.qkv_prefill_graph_create([plan] * w.n_layers, layers, w.nt, stream)
+    for _ in range(max(args.warmup, 3)):
+        graph.launch(stream)
+    stream.synchronize()
+    flags, _ = Q.qkv_check_device_error(stream)
+    if flags:
+        raise RuntimeError("device status flags set during warm-up: %#x" % flags)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    barrier_sync(world)
+    elapsed = time_replays(lambda: graph.launch(stream), args.steps, stream)
+    barrier_sync(world)
+    clk = clocks.stop()
+    elapsed = max_over_ranks(elapsed, world)
+    per_layer = elapsed / args.steps / w.n_layers
+    algo_b, algo_f = prefill_algo(w)
+    peak, peak_kind = measured_peak()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": world * w.n_layers * args.steps / elapsed, "unit": "layers/s",
+            "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+            "ms_per_step": 1e3 * elapsed / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 x bf16 -> f32",
+            "data": "synthetic (seeded SplitMix64/Box-Muller X ~N(0,1), W ~N(0,0.02), bias ~N(0,0.1))",
+            "config": dict(workload_config(w), nt=w.nt, positions="0..%d" % (w.nt - 1)),
+            "hbm_gbs": algo_b / per_layer / 1e9, "tflops": algo_f / per_layer / 1e12,
+            "roofline": {"bound": "hbm", "achieved": algo_b / per_layer / 1e9, "peak": peak, "unit": "GB/s",
+                         "frac": algo_b / per_layer / 1e9 / peak, "peak_kind": peak_kind,
+                         "frac_of_nominal_8000": algo_b / per_layer / 1e9 / NOMINAL_HBM_GBS,
+                         "traffic": None, "algo_bytes_per_launch": algo_b, "algo_flops_per_launch": algo_f,
+                         "kernel": "qkv_prefill_kernel (tcgen05 bf16 GEMM + bias/RoPE/KV-store epilogue)",
+                         "duration_basis": "step time / %d launches" % w.n_layers},
+            "gpu_launches": graph.kernel_count * args.steps, "launches_per_step": graph.kernel_count,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
     w = configs.WORKLOADS[args.workload]
@@ -390,6 +470,8 @@ def main():
                                 mixed_layers=tuple(l for l in w.mixed_layers if l < args.layers))
     if args.impl == "reference":
         reference_arm(args, w)
+    elif w.nt > 1:
+        prefill_arm(args, w)
     else:
         native_arm(args, w)
 

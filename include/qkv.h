@@ -251,6 +251,27 @@ qkv_status qkv_model_graph_launch(qkv_graph* graph, void* stream);
 qkv_status qkv_model_graph_run_host(qkv_graph* graph, const void* h_in, void* d_in,
                                     size_t in_bytes, const void* d_out, void* h_out,
                                     size_t out_bytes, void* stream);
+/* Per-layer buffers of a prefill graph layer (concat class, bf16 weights):
+ * X [nt x H] bf16, w [R x H] bf16, bias [R], positions [nt] int32 (device),
+ * Y [nt x R] f32, and the layer's cache regions — as in qkv_prefill_step. */
+typedef struct qkv_prefill_ptrs {
+    const uint16_t* X;
+    const void* w;
+    const float* bias;
+    const int32_t* positions;
+    float* Y;
+    void* kv_k;
+    void* kv_v;
+} qkv_prefill_ptrs;
+
+/* Capture n_layers prefill steps of nt tokens (plans[i] with layers[i]) into a
+ * CUDA graph, chained with programmatic dependent launch; replay it with
+ * qkv_model_graph_launch.  Errors as qkv_model_graph_create and
+ * qkv_prefill_step. */
+qkv_status qkv_prefill_graph_create(const qkv_plan* const* plans, int32_t n_layers,
+                                    const qkv_prefill_ptrs* layers, int32_t nt, void* stream,
+                                    qkv_graph** out);
+
 /* Number of kernel nodes in the graph (launches per decode step). */
 qkv_status qkv_model_graph_kernel_count(const qkv_graph* graph, int32_t* out);
 void qkv_model_graph_destroy(qkv_graph* graph);

@@ -69,6 +69,10 @@ class qkv_layer_ptrs(ctypes.Structure):
                  "kv_k", "kv_v")]
 
 
+class qkv_prefill_ptrs(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("X", "w", "bias", "positions", "Y", "kv_k", "kv_v")]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -113,6 +117,7 @@ def _declare(lib):
         "kv_cache_view": ([vp, vp, vp, ctypes.POINTER(qkv_kv_view)], st),
         "qkv_model_graph_create": ([vp, i32, vp, vp, vp, ctypes.POINTER(vp)], st),
         "qkv_model_graph_launch": ([vp, vp], st),
+        "qkv_prefill_graph_create": ([vp, i32, vp, i32, vp, ctypes.POINTER(vp)], st),
         "qkv_model_graph_run_host": ([vp, vp, vp, sz, vp, vp, sz, vp], st),
         "qkv_model_graph_kernel_count": ([vp, ctypes.POINTER(i32)], st),
         "qkv_model_graph_destroy": ([vp], None),
@@ -292,6 +297,20 @@ def qkv_model_graph_create(plans, layers, d_pos, stream) -> ModelGraph:
     _check(_lib.qkv_model_graph_create(arr_plans, n, arr_layers, _ptr(d_pos), _stream(stream),
                                        ctypes.byref(h)))
     return ModelGraph(h.value, (plans, layers, d_pos))
+
+
+def qkv_prefill_graph_create(plans, layers, nt: int, stream) -> ModelGraph:
+    """``layers``: list of dicts with the qkv_prefill_ptrs field names -> tensors."""
+    n = len(plans)
+    assert len(layers) == n
+    arr_plans = (ctypes.c_void_p * n)(*[p.handle for p in plans])
+    arr_layers = (qkv_prefill_ptrs * n)()
+    for i, L in enumerate(layers):
+        for name, _ in qkv_prefill_ptrs._fields_:
+            setattr(arr_layers[i], name, _ptr(L.get(name)))
+    h = ctypes.c_void_p()
+    _check(_lib.qkv_prefill_graph_create(arr_plans, n, arr_layers, nt, _stream(stream), ctypes.byref(h)))
+    return ModelGraph(h.value, (plans, layers))
 
 
 # ---------------------------------------------------------------- device status

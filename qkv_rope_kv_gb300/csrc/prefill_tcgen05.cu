@@ -36,10 +36,21 @@ constexpr int kBN = 64;                        // weight rows per tile (UMMA N)
 constexpr int kBox = 32;                       // rows per W box
 constexpr int kBK = 64;                        // K per stage (bf16): 128 bytes
 constexpr int kUK = 16;                        // K per tcgen05.mma, kind::f16
-constexpr int kStages = 6;
+#ifndef QKV_PREFILL_KSUB
+#define QKV_PREFILL_KSUB 2
+#endif
+#ifndef QKV_PREFILL_STAGES
+#define QKV_PREFILL_STAGES 4
+#endif
+// A stage holds kSub consecutive 64-wide K blocks, so each weight row is
+// requested kSub * 128 contiguous bytes at a time.
+constexpr int kSub = QKV_PREFILL_KSUB;
+constexpr int kStages = QKV_PREFILL_STAGES;
 constexpr int kThreads = 128;
-constexpr uint32_t kABytes = kBM * kBK * 2;    // 16 KB
-constexpr uint32_t kBBytes = kBN * kBK * 2;    // 8 KB
+constexpr uint32_t kABlk = kBM * kBK * 2;      // 16 KB: one X block (128 x 64)
+constexpr uint32_t kBBlk = kBN * kBK * 2;      // 8 KB: one W block (64 x 64)
+constexpr uint32_t kABytes = kSub * kABlk;     // X bytes per stage
+constexpr uint32_t kBBytes = kSub * kBBlk;     // W bytes per stage
 constexpr uint32_t kBoxBytes = kBox * kBK * 2; // 4 KB
 constexpr uint32_t kTmemCols = 64;             // f32 accumulator columns (= kBN)
 constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStages * (kABytes + kBBytes) +
@@ -176,7 +187,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         rowB = rowA + kBox;
     }
     const int base = sec == 0 ? 0 : (sec == 1 ? p.nqt : p.nqt + p.nkt);  // section's first global row
-    const int nk = (p.H + kBK - 1) / kBK;
+    const int nk = (p.H + kSub * kBK - 1) / (kSub * kBK);  // stages of kSub K blocks
+    // CTAs start their K loop at different blocks, so the X tiles they read at
+    // any moment are spread over L2 instead of every CTA hitting the same lines.
+#ifndef QKV_PREFILL_STAGGER
+#define QKV_PREFILL_STAGGER 1
+#endif
+    const int k_first = QKV_PREFILL_STAGGER ? static_cast<int>((static_cast<long long>(tile) * nk) / gridDim.x) : 0;
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -200,6 +217,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
+    // X, positions and the outputs may belong to the preceding grid in the
+    // stream: wait for it before any of them is touched; the next grid may be
+    // scheduled now (it waits for this one in the same way).
+    griddep_wait();
+    griddep_launch_dependents();
 
     if (warp == 0 && lane == 0) {
         // ---- producer: TMA tiles of X (128 x 64) and W (two 32 x 64 boxes) per stage ----
@@ -212,10 +234,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 flag_timeout();
                 break;
             }
+            const int kx = (k_first + kb) % nk;  // stage index along K
             mbar_arrive_expect_tx(&full[s], kABytes + kBBytes);
-            tma_load_2d(sA + s * kABytes, &tm_x, kb * kBK, m0, &full[s]);
-            tma_load_2d(sB + s * kBBytes, &tm_w, kb * kBK, base + rowA, &full[s]);
-            tma_load_2d(sB + s * kBBytes + kBoxBytes, &tm_w, kb * kBK, base + rowB, &full[s]);
+#pragma unroll
+            for (int j = 0; j < kSub; ++j) {
+                const int kc = (kx * kSub + j) * kBK;  // element column of this 64-wide block
+                unsigned char* b = sB + s * kBBytes + j * kBBlk;
+                tma_load_2d(b, &tm_w, kc, base + rowA, &full[s]);
+                tma_load_2d(b + kBoxBytes, &tm_w, kc, base + rowB, &full[s]);
+            }
+#pragma unroll
+            for (int j = 0; j < kSub; ++j)
+                tma_load_2d(sA + s * kABytes + j * kABlk, &tm_x, (kx * kSub + j) * kBK, m0, &full[s]);
             ++issued;
         }
         // Drain: no copy may still be landing in shared memory when the CTA exits.
@@ -231,11 +261,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            const unsigned char* a = sA + s * kABytes;
-            const unsigned char* b = sB + s * kBBytes;
 #pragma unroll
-            for (int k = 0; k < kBK / kUK; ++k)
-                tc_mma(tmem, smem_desc_k128(a + k * kUK * 2), smem_desc_k128(b + k * kUK * 2), (kb | k) != 0);
+            for (int j = 0; j < kSub; ++j) {
+                const unsigned char* a = sA + s * kABytes + j * kABlk;
+                const unsigned char* b = sB + s * kBBytes + j * kBBlk;
+#pragma unroll
+                for (int k = 0; k < kBK / kUK; ++k)
+                    tc_mma(tmem, smem_desc_k128(a + k * kUK * 2), smem_desc_k128(b + k * kUK * 2),
+                           (kb | j | k) != 0);
+            }
             tc_commit(&empty[s]);  // the stage is free once these MMAs have read it
         }
         tc_commit(done);  // arrives when every MMA issued above has completed
@@ -334,7 +368,7 @@ bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 
 }  // namespace
 
-qkv_status launch_prefill(const PrefillParams& p, cudaStream_t stream, const char** why) {
+qkv_status launch_prefill(const PrefillParams& p, bool pdl, cudaStream_t stream, const char** why) {
     if (p.hd % kBN != 0) {
         *why = "head_dim must be a multiple of 64 (two 32-row boxes per neox tile)";
         return QKV_ERR_UNSUPPORTED;
@@ -364,9 +398,17 @@ qkv_status launch_prefill(const PrefillParams& p, cudaStream_t stream, const cha
         *why = cudaGetErrorString(e);
         return QKV_ERR_CUDA;
     }
-    const dim3 grid(R / kBN, (p.nt + kBM - 1) / kBM);
-    qkv_prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_x, tm_w, p);
-    e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(R / kBN, (p.nt + kBM - 1) / kBM);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, qkv_prefill_kernel, tm_x, tm_w, p);
     if (e != cudaSuccess) {
         *why = cudaGetErrorString(e);
         return QKV_ERR_CUDA;

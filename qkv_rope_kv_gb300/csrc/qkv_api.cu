@@ -312,10 +312,10 @@ extern "C" qkv_status qkv_chain_store(const qkv_plan* plan, const float* src, vo
 
 // ------------------------------------------------------------------ prefill
 
-extern "C" qkv_status qkv_prefill_step(const qkv_plan* plan, const uint16_t* X, int32_t nt,
-                                       const void* w, const float* bias,
-                                       const int32_t* d_positions, float* Y, void* kv_k,
-                                       void* kv_v, void* stream) {
+namespace {
+
+qkv_status check_prefill(const qkv_plan* plan, int32_t nt, const uint16_t* X, const void* w, const float* bias,
+                         const int32_t* d_positions, const float* Y, const void* kv_k, const void* kv_v) {
     REQUIRE(plan, "plan is null");
     REQUIRE(nt >= 0, "nt must be >= 0");
     REQUIRE(X && w && bias && d_positions && Y && kv_k && kv_v, "null pointer");
@@ -323,6 +323,12 @@ extern "C" qkv_status qkv_prefill_step(const qkv_plan* plan, const uint16_t* X, 
         return fail(QKV_ERR_UNSUPPORTED, "prefill needs bf16 weights (tensor-core bf16 x bf16)");
     if (plan->d.layer_class != QKV_CLASS_CONCAT)
         return fail(QKV_ERR_UNSUPPORTED, "prefill takes the concat weight matrix");
+    return QKV_OK;
+}
+
+qkv_status run_prefill(const qkv_plan* plan, const uint16_t* X, int32_t nt, const void* w, const float* bias,
+                       const int32_t* d_positions, float* Y, void* kv_k, void* kv_v, bool pdl,
+                       cudaStream_t stream) {
     if (nt == 0) return QKV_OK;
     PrefillParams p;
     std::memset(&p, 0, sizeof p);
@@ -342,9 +348,20 @@ extern "C" qkv_status qkv_prefill_step(const qkv_plan* plan, const uint16_t* X, 
     p.kv_f16 = plan->d.kv_dtype == QKV_F16 ? 1 : 0;
     std::memcpy(p.inv_freq, plan->inv_freq, sizeof p.inv_freq);
     const char* why = nullptr;
-    qkv_status st = launch_prefill(p, static_cast<cudaStream_t>(stream), &why);
+    qkv_status st = launch_prefill(p, pdl, stream, &why);
     if (st != QKV_OK) return fail(st, "prefill: %s", why ? why : "launch failed");
     return QKV_OK;
+}
+
+}  // namespace
+
+extern "C" qkv_status qkv_prefill_step(const qkv_plan* plan, const uint16_t* X, int32_t nt,
+                                       const void* w, const float* bias,
+                                       const int32_t* d_positions, float* Y, void* kv_k,
+                                       void* kv_v, void* stream) {
+    qkv_status st = check_prefill(plan, nt, X, w, bias, d_positions, Y, kv_k, kv_v);
+    if (st != QKV_OK) return st;
+    return run_prefill(plan, X, nt, w, bias, d_positions, Y, kv_k, kv_v, false, static_cast<cudaStream_t>(stream));
 }
 
 // ------------------------------------------------------------------ cache view
@@ -368,6 +385,10 @@ struct qkv_graph {
     cudaGraphExec_t exec = nullptr;
     int32_t kernels = 0;
 };
+
+namespace {
+qkv_status finish_capture(cudaStream_t s, qkv_status st, qkv_graph** out);
+}
 
 extern "C" qkv_status qkv_model_graph_create(const qkv_plan* const* plans, int32_t n_layers,
                                              const qkv_layer_ptrs* layers, const int32_t* d_pos,
@@ -418,8 +439,16 @@ extern "C" qkv_status qkv_model_graph_create(const qkv_plan* const* plans, int32
         }
         st = run_decode(p, L.x, ws, bs, d_pos, L.q, L.k, L.v, L.kv_k, L.kv_v, i > 0, s);
     }
+    return finish_capture(s, st, out);
+}
+
+namespace {
+
+// End a capture started by one of the graph builders, count its kernel nodes and
+// instantiate it.  `st` is the status of the launches made during the capture.
+qkv_status finish_capture(cudaStream_t s, qkv_status st, qkv_graph** out) {
     cudaGraph_t graph = nullptr;
-    e = cudaStreamEndCapture(s, &graph);
+    cudaError_t e = cudaStreamEndCapture(s, &graph);
     if (st != QKV_OK) {
         if (graph) cudaGraphDestroy(graph);
         return st;
@@ -461,6 +490,33 @@ extern "C" qkv_status qkv_model_graph_create(const qkv_plan* const* plans, int32
     g->kernels = kernels;
     *out = g;
     return QKV_OK;
+}
+
+}  // namespace
+
+extern "C" qkv_status qkv_prefill_graph_create(const qkv_plan* const* plans, int32_t n_layers,
+                                               const qkv_prefill_ptrs* layers, int32_t nt, void* stream,
+                                               qkv_graph** out) {
+    REQUIRE(out, "out is null");
+    *out = nullptr;
+    REQUIRE(plans && layers, "null argument");
+    REQUIRE(n_layers >= 1, "n_layers must be >= 1");
+    REQUIRE(nt >= 1, "nt must be >= 1");
+    REQUIRE(stream, "capture needs a non-default stream");
+    for (int32_t i = 0; i < n_layers; ++i) {
+        const qkv_prefill_ptrs& L = layers[i];
+        qkv_status st = check_prefill(plans[i], nt, L.X, L.w, L.bias, L.positions, L.Y, L.kv_k, L.kv_v);
+        if (st != QKV_OK) return fail(st, "layer %d: %s", i, g_last_error.c_str());
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamBeginCapture");
+    qkv_status st = QKV_OK;
+    for (int32_t i = 0; i < n_layers && st == QKV_OK; ++i) {
+        const qkv_prefill_ptrs& L = layers[i];
+        st = run_prefill(plans[i], L.X, nt, L.w, L.bias, L.positions, L.Y, L.kv_k, L.kv_v, i > 0, s);
+    }
+    return finish_capture(s, st, out);
 }
 
 extern "C" qkv_status qkv_model_graph_launch(qkv_graph* g, void* stream) {

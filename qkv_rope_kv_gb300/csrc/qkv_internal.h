@@ -52,5 +52,5 @@ struct PrefillParams {
     int32_t nt, H, nqt, nkt, hd, n_ctx, kv_f16;
     float inv_freq[QKV_MAX_HEAD_DIM / 2];
 };
-qkv_status launch_prefill(const PrefillParams& p, cudaStream_t stream, const char** why);
+qkv_status launch_prefill(const PrefillParams& p, bool pdl, cudaStream_t stream, const char** why);
 cudaError_t prefill_status_read(cudaStream_t stream, uint32_t* flags, int32_t* bad_pos);

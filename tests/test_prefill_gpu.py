@@ -162,3 +162,35 @@ def test_qwen14b_prefill_nt128_48_layers(orc, qkv):
                               tokens=tokens)
         check(w.n_head, w.n_head_kv, w.head_dim, got, want, positions, "14B prefill layer %d" % layer)
     assert Q.qkv_check_device_error()[0] == 0
+
+
+def test_prefill_graph_equals_sequential_calls(qkv):
+    """Three prefill layers captured in one graph (PDL-chained) give the bits of three
+    separate qkv_prefill_step calls; the graph has one kernel per layer."""
+    import torch
+    nt, H, nh, nkv, hd, n_ctx, L = 64, 512, 4, 2, 64, 128, 3
+    R = (nh + 2 * nkv) * hd
+    plan = Q.qkv_plan_create(H, nh, nkv, hd, 1e6, n_ctx, w_dtype=Q.QKV_BF16, kv_dtype=Q.QKV_F16)
+    positions = torch.arange(10, 10 + nt, dtype=torch.int32, device="cuda")
+    layers = []
+    for l in range(L):
+        layers.append(dict(X=to_dev(synth.prefill_x(0, 40 + l, nt, H)), w=to_dev(synth.weight_rows(0, 40 + l, 0, R, H, "bf16")),
+                           bias=to_dev(synth.bias(0, 40 + l, R)), positions=positions,
+                           Y=torch.zeros(nt, R, dtype=torch.float32, device="cuda"),
+                           kv_k=torch.zeros(n_ctx, nkv * hd, dtype=torch.int16, device="cuda"),
+                           kv_v=torch.zeros(n_ctx, nkv * hd, dtype=torch.int16, device="cuda")))
+    stream = torch.cuda.Stream()
+    g = Q.qkv_prefill_graph_create([plan] * L, layers, nt, stream)
+    assert g.kernel_count == L
+    g.launch(stream)
+    stream.synchronize()
+    first = [(to_host(d["Y"]).copy(), to_host(d["kv_k"]).copy(), to_host(d["kv_v"]).copy()) for d in layers]
+    for d in layers:
+        d["Y"].zero_(); d["kv_k"].zero_(); d["kv_v"].zero_()
+    torch.cuda.synchronize()
+    for d in layers:
+        Q.qkv_prefill_step(plan, d["X"], nt, d["w"], d["bias"], d["positions"], d["Y"], d["kv_k"], d["kv_v"])
+    torch.cuda.synchronize()
+    for d, (y, k, v) in zip(layers, first):
+        assert np.array_equal(to_host(d["Y"]).view(np.uint32), y.view(np.uint32))
+        assert np.array_equal(to_host(d["kv_k"]), k) and np.array_equal(to_host(d["kv_v"]), v)
