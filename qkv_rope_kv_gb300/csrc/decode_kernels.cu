@@ -314,10 +314,10 @@ __global__ void __launch_bounds__(256) qkv_decode_kernel(const __grid_constant__
 // on H and G, not on the layer class, so concat and mixed layers give
 // identical bits.
 #ifndef QKV_DECODE_GROUPS
-#define QKV_DECODE_GROUPS 4
+#define QKV_DECODE_GROUPS 5
 #endif
 #ifndef QKV_DECODE_GROUP_WARPS
-#define QKV_DECODE_GROUP_WARPS 2
+#define QKV_DECODE_GROUP_WARPS 3
 #endif
 constexpr int kGroups = QKV_DECODE_GROUPS;            // NG: consumer groups (stage owners)
 constexpr int kGroupWarps = QKV_DECODE_GROUP_WARPS;   // G: warps per group
@@ -425,8 +425,11 @@ __device__ __forceinline__ void dot2_staged(const unsigned char* row0, const uns
     a1 = warp_sum(__fadd_rn(c1.x, c1.y));
 }
 
+#ifndef QKV_DECODE_CTAS_PER_SM
+#define QKV_DECODE_CTAS_PER_SM 1
+#endif
 template <typename WT, int MODE>
-__global__ void __launch_bounds__(kTmaThreads, 1)
+__global__ void __launch_bounds__(kTmaThreads, QKV_DECODE_CTAS_PER_SM)
     qkv_decode_tma_kernel(const __grid_constant__ DecodeParams p, int stages, uint32_t stage_bytes,
                           uint32_t x_bytes) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -682,7 +685,8 @@ cudaError_t launch_decode_tma(const DecodeParams& p, int stages, uint32_t stage_
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int units = unit_count(p.nqt, p.nkt, p.hd);
-    const int grid = units < sm_count() ? units : sm_count();
+    const int ctas = sm_count() * QKV_DECODE_CTAS_PER_SM;
+    const int grid = units < ctas ? units : ctas;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kTmaThreads);

@@ -19,7 +19,10 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 constexpr uint64_t kWaitTimeoutNs = 500ull * 1000ull * 1000ull;  // 0.5 s: far beyond any healthy wait
 // A waiting thread sleeps until the phase completes or this hint elapses,
 // instead of spinning and taking issue slots from working warps.
-constexpr uint32_t kTryWaitSuspendNs = 20000u;
+#ifndef QKV_TRY_WAIT_SUSPEND_NS
+#define QKV_TRY_WAIT_SUSPEND_NS 20000u
+#endif
+constexpr uint32_t kTryWaitSuspendNs = QKV_TRY_WAIT_SUSPEND_NS;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
