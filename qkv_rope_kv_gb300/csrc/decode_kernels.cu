@@ -76,12 +76,12 @@ __device__ __forceinline__ void flag_bad_pos(int pos) {
 
 __device__ __forceinline__ void flag_timeout() { atomicOr(&g_qkv_status[0], kFlagTimeout); }
 
-// q (sec 0) or k (sec 1) pair: bias, rotate, write back; k also goes to the cache.
-__device__ __forceinline__ void epi_qk_pair(const DecodeParams& p, int sec, int j, int j2, float y0,
-                                            float y1, int pos, float inv_freq, bool store) {
-    const float* b = p.bias[sec];
-    const float x0 = __fadd_rn(y0, b[j]);
-    const float x1 = __fadd_rn(y1, b[j2]);
+// q (sec 0) or k (sec 1) pair: bias (b0, b1 already loaded), rotate, write back;
+// k also goes to the cache.
+__device__ __forceinline__ void epi_qk_pair_b(const DecodeParams& p, int sec, int j, int j2, float y0, float y1,
+                                              float b0, float b1, int pos, float inv_freq, bool store) {
+    const float x0 = __fadd_rn(y0, b0);
+    const float x1 = __fadd_rn(y1, b1);
     float r0, r1;
     rope_rotate(x0, x1, rope_theta(pos, inv_freq), r0, r1);
     float* o = p.out[sec];
@@ -94,11 +94,20 @@ __device__ __forceinline__ void epi_qk_pair(const DecodeParams& p, int sec, int 
     }
 }
 
-// v element: bias, write back, store to the cache.
-__device__ __forceinline__ void epi_v_elem(const DecodeParams& p, int j, float y, int pos, bool store) {
-    const float val = __fadd_rn(y, p.bias[2][j]);
+__device__ __forceinline__ void epi_qk_pair(const DecodeParams& p, int sec, int j, int j2, float y0, float y1,
+                                            int pos, float inv_freq, bool store) {
+    epi_qk_pair_b(p, sec, j, j2, y0, y1, p.bias[sec][j], p.bias[sec][j2], pos, inv_freq, store);
+}
+
+// v element: bias (already loaded), write back, store to the cache.
+__device__ __forceinline__ void epi_v_elem_b(const DecodeParams& p, int j, float y, float b, int pos, bool store) {
+    const float val = __fadd_rn(y, b);
     p.out[2][j] = val;
     if (store) kv_put(p.kv_v, p.kv_f16, static_cast<size_t>(pos) * static_cast<size_t>(p.nkt) + j, val);
+}
+
+__device__ __forceinline__ void epi_v_elem(const DecodeParams& p, int j, float y, int pos, bool store) {
+    epi_v_elem_b(p, j, y, p.bias[2][j], pos, store);
 }
 
 // ---------------------------------------------------------------- projection
@@ -313,16 +322,16 @@ __global__ void __launch_bounds__(256) qkv_decode_kernel(const __grid_constant__
 // then the G warp partials are added in warp order.  The order depends only
 // on H and G, not on the layer class, so concat and mixed layers give
 // identical bits.
-#ifndef QKV_DECODE_GROUPS
-#define QKV_DECODE_GROUPS 5
-#endif
 #ifndef QKV_DECODE_GROUP_WARPS
-#define QKV_DECODE_GROUP_WARPS 3
+#define QKV_DECODE_GROUP_WARPS 1
 #endif
-constexpr int kGroups = QKV_DECODE_GROUPS;            // NG: consumer groups (stage owners)
 constexpr int kGroupWarps = QKV_DECODE_GROUP_WARPS;   // G: warps per group
-constexpr int kConsumerWarps = kGroups * kGroupWarps;
-constexpr int kTmaThreads = (kConsumerWarps + 1) * 32;
+// Launch shapes: rows of >= 8 KB (one neox pair per stage is >= 16 KB) use one
+// CTA per SM with 5 consumer groups; shorter rows use two CTAs per SM with 3
+// groups each, which keeps more independent producers streaming.
+constexpr int kGroupsLarge = 5;
+constexpr int kGroupsSmall = 3;
+constexpr size_t kSmallRowBytes = 8192;
 
 #ifndef QKV_DECODE_PAIRS
 #define QKV_DECODE_PAIRS 1
@@ -425,13 +434,11 @@ __device__ __forceinline__ void dot2_staged(const unsigned char* row0, const uns
     a1 = warp_sum(__fadd_rn(c1.x, c1.y));
 }
 
-#ifndef QKV_DECODE_CTAS_PER_SM
-#define QKV_DECODE_CTAS_PER_SM 1
-#endif
-template <typename WT, int MODE>
-__global__ void __launch_bounds__(kTmaThreads, QKV_DECODE_CTAS_PER_SM)
+template <typename WT, int MODE, int kGroups>
+__global__ void __launch_bounds__((kGroups * kGroupWarps + 1) * 32, 2)
     qkv_decode_tma_kernel(const __grid_constant__ DecodeParams p, int stages, uint32_t stage_bytes,
                           uint32_t x_bytes) {
+    constexpr int kConsumerWarps = kGroups * kGroupWarps;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float freq_s[QKV_MAX_HEAD_DIM / 2];
     __shared__ float gpart[kGroups][kGroupWarps][2];
@@ -523,6 +530,13 @@ __global__ void __launch_bounds__(kTmaThreads, QKV_DECODE_CTAS_PER_SM)
         const unsigned char* st = ring + static_cast<size_t>(s) * stage_bytes;
         const uint32_t blk = static_cast<uint32_t>(t.n) * row_bytes;
         for (int j = 0; j < t.n; ++j) {
+            const int r0 = t.r + j, r1 = t.r + t.off + j;
+            // the epilogue's bias loads are issued now and land during the dot product
+            float b0 = 0.f, b1 = 0.f;
+            if (MODE == kFused && gw == 0 && lane == 0) {
+                b0 = __ldg(p.bias[t.sec] + r0);
+                b1 = __ldg(p.bias[t.sec] + r1);
+            }
             float a0, a1;
             dot2_staged<WT>(st + j * row_bytes, st + blk + j * row_bytes, xs4, p.H, gt, a0, a1);
             const bool last = (j == t.n - 1);
@@ -548,15 +562,14 @@ __global__ void __launch_bounds__(kTmaThreads, QKV_DECODE_CTAS_PER_SM)
             }
             if (last && gw == 0 && lane == 0) mbar_arrive(&empty[s]);
             if (gw == 0 && lane == 0) {
-                const int r0 = t.r + j, r1 = t.r + t.off + j;
                 if constexpr (MODE == kProjectOnly) {
                     p.out[t.sec][r0] = a0;
                     p.out[t.sec][r1] = a1;
                 } else if (t.sec < 2) {
-                    epi_qk_pair(p, t.sec, r0, r1, a0, a1, pos, freq_s[r0 % p.hd], store);
+                    epi_qk_pair_b(p, t.sec, r0, r1, a0, a1, b0, b1, pos, freq_s[r0 % p.hd], store);
                 } else {
-                    epi_v_elem(p, r0, a0, pos, store);
-                    epi_v_elem(p, r1, a1, pos, store);
+                    epi_v_elem_b(p, r0, a0, b0, pos, store);
+                    epi_v_elem_b(p, r1, a1, b1, pos, store);
                 }
             }
         }
@@ -653,43 +666,50 @@ int sm_count() {
 
 // Dynamic shared memory per CTA: the ring takes what one CTA per SM can have,
 // which keeps the most weight bytes in flight.
-#ifndef QKV_DECODE_SMEM_KB
-#define QKV_DECODE_SMEM_KB 225
+#ifndef QKV_DECODE_MAX_STAGES
+#define QKV_DECODE_MAX_STAGES 32
 #endif
-// Dynamic shared memory per CTA for x plus the ring (one CTA per SM).
-constexpr size_t kSmemBudget = QKV_DECODE_SMEM_KB * 1024;
-constexpr int kMaxStages = 32;
+constexpr int kMaxStages = QKV_DECODE_MAX_STAGES;
 
-// Stages of the ring for this shape (a multiple of the consumer count), or 0
-// when the shape needs the register-streaming kernel (unaligned rows, or rows
-// too long to stage).
+struct RingShape {
+    int stages;        // multiple of the group count
+    int ctas_per_sm;
+    uint32_t stage_bytes, x_bytes;
+};
+
+// Ring for this layer, or stages = 0 when the shape needs the register-streaming
+// kernel (unaligned rows, or rows too long to stage).  Dynamic shared memory:
+// 225 KB for one CTA per SM, 110 KB each for two.
 template <typename WT>
-int tma_stages(const DecodeParams& p, uint32_t& stage_bytes, uint32_t& x_bytes) {
+RingShape ring_shape(const DecodeParams& p, int groups, int ctas_per_sm) {
+    RingShape r = {};
     const size_t row = static_cast<size_t>(p.H) * sizeof(WT);
-    stage_bytes = static_cast<uint32_t>((2 * kPairs * row + 127) / 128 * 128);
-    x_bytes = static_cast<uint32_t>((static_cast<size_t>(p.H) * 4 + 127) / 128 * 128);
-    const size_t barriers = 2 * kMaxStages * sizeof(uint64_t);
-    if (x_bytes + barriers + static_cast<size_t>(kGroups) * stage_bytes > kSmemBudget) return 0;
-    int st = static_cast<int>((kSmemBudget - x_bytes - barriers) / stage_bytes);
+    const size_t budget = ctas_per_sm == 1 ? 225 * 1024 : 110 * 1024;
+    r.ctas_per_sm = ctas_per_sm;
+    r.stage_bytes = static_cast<uint32_t>((2 * kPairs * row + 127) / 128 * 128);
+    r.x_bytes = static_cast<uint32_t>((static_cast<size_t>(p.H) * 4 + 127) / 128 * 128);
+    const size_t barriers = 2 * 32 * sizeof(uint64_t);
+    if (r.x_bytes + barriers + static_cast<size_t>(groups) * r.stage_bytes > budget) return r;
+    int st = static_cast<int>((budget - r.x_bytes - barriers) / r.stage_bytes);
     st = st > kMaxStages ? kMaxStages : st;
-    st -= st % kGroups;
-    return st;
+    st -= st % groups;
+    r.stages = st;
+    return r;
 }
 
-template <typename WT, int MODE>
-cudaError_t launch_decode_tma(const DecodeParams& p, int stages, uint32_t stage_bytes, uint32_t x_bytes,
-                              bool pdl, cudaStream_t stream) {
-    auto kernel = qkv_decode_tma_kernel<WT, MODE>;
-    const size_t smem = x_bytes + static_cast<size_t>(stages) * stage_bytes + 2 * stages * sizeof(uint64_t);
+template <typename WT, int MODE, int kGroups>
+cudaError_t launch_decode_tma(const DecodeParams& p, const RingShape& r, bool pdl, cudaStream_t stream) {
+    auto kernel = qkv_decode_tma_kernel<WT, MODE, kGroups>;
+    const size_t smem = r.x_bytes + static_cast<size_t>(r.stages) * r.stage_bytes + 2 * r.stages * sizeof(uint64_t);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int units = unit_count(p.nqt, p.nkt, p.hd);
-    const int ctas = sm_count() * QKV_DECODE_CTAS_PER_SM;
+    const int ctas = sm_count() * r.ctas_per_sm;
     const int grid = units < ctas ? units : ctas;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kTmaThreads);
+    cfg.blockDim = dim3((kGroups * kGroupWarps + 1) * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -697,15 +717,20 @@ cudaError_t launch_decode_tma(const DecodeParams& p, int stages, uint32_t stage_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kernel, p, stages, stage_bytes, x_bytes);
+    return cudaLaunchKernelEx(&cfg, kernel, p, r.stages, r.stage_bytes, r.x_bytes);
 }
 
 template <typename WT, bool VEC, int MODE>
 cudaError_t launch_decode_t(const DecodeParams& p, bool pdl, cudaStream_t stream) {
     if constexpr (VEC) {
-        uint32_t stage_bytes = 0, x_bytes = 0;
-        const int st = tma_stages<WT>(p, stage_bytes, x_bytes);
-        if (st > 0) return launch_decode_tma<WT, MODE>(p, st, stage_bytes, x_bytes, pdl, stream);
+        const size_t row = static_cast<size_t>(p.H) * sizeof(WT);
+        if (row >= kSmallRowBytes) {
+            const RingShape r = ring_shape<WT>(p, kGroupsLarge, 1);
+            if (r.stages > 0) return launch_decode_tma<WT, MODE, kGroupsLarge>(p, r, pdl, stream);
+        } else {
+            const RingShape r = ring_shape<WT>(p, kGroupsSmall, 2);
+            if (r.stages > 0) return launch_decode_tma<WT, MODE, kGroupsSmall>(p, r, pdl, stream);
+        }
     }
     auto kernel = qkv_decode_kernel<WT, VEC, MODE>;
     const size_t smem = static_cast<size_t>(p.H) * sizeof(float);
