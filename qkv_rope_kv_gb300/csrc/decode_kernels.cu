@@ -78,10 +78,9 @@ __device__ __forceinline__ void flag_timeout() { atomicOr(&g_qkv_status[0], kFla
 
 // q (sec 0) or k (sec 1) pair: bias (b0, b1 already loaded), rotate, write back;
 // k also goes to the cache.
-__device__ __forceinline__ void epi_qk_pair_b(const DecodeParams& p, int sec, int j, int j2, float y0, float y1,
-                                              float b0, float b1, int pos, float inv_freq, bool store) {
-    const float x0 = __fadd_rn(y0, b0);
-    const float x1 = __fadd_rn(y1, b1);
+// q/k pair (j, j2) after the bias: rotate, write back, store k rows to the cache.
+__device__ __forceinline__ void epi_qk_rot(const DecodeParams& p, int sec, int j, int j2, float x0, float x1,
+                                           int pos, float inv_freq, bool store) {
     float r0, r1;
     rope_rotate(x0, x1, rope_theta(pos, inv_freq), r0, r1);
     float* o = p.out[sec];
@@ -92,6 +91,11 @@ __device__ __forceinline__ void epi_qk_pair_b(const DecodeParams& p, int sec, in
         kv_put(p.kv_k, p.kv_f16, row + j, r0);
         kv_put(p.kv_k, p.kv_f16, row + j2, r1);
     }
+}
+
+__device__ __forceinline__ void epi_qk_pair_b(const DecodeParams& p, int sec, int j, int j2, float y0, float y1,
+                                              float b0, float b1, int pos, float inv_freq, bool store) {
+    epi_qk_rot(p, sec, j, j2, __fadd_rn(y0, b0), __fadd_rn(y1, b1), pos, inv_freq, store);
 }
 
 __device__ __forceinline__ void epi_qk_pair(const DecodeParams& p, int sec, int j, int j2, float y0, float y1,
@@ -329,8 +333,26 @@ constexpr int kGroupWarps = QKV_DECODE_GROUP_WARPS;   // G: warps per group
 // Launch shapes: rows of >= 8 KB (one neox pair per stage is >= 16 KB) use one
 // CTA per SM with 5 consumer groups; shorter rows use two CTAs per SM with 3
 // groups each, which keeps more independent producers streaming.
-constexpr int kGroupsLarge = 5;
-constexpr int kGroupsSmall = 3;
+#ifndef QKV_DECODE_LARGE_GROUPS
+#define QKV_DECODE_LARGE_GROUPS 5
+#endif
+#ifndef QKV_DECODE_LARGE_CTAS
+#define QKV_DECODE_LARGE_CTAS 1
+#endif
+#ifndef QKV_DECODE_LARGE_SMEM_KB
+#define QKV_DECODE_LARGE_SMEM_KB 225
+#endif
+#ifndef QKV_DECODE_SMALL_GROUPS
+#define QKV_DECODE_SMALL_GROUPS 3
+#endif
+#ifndef QKV_DECODE_SMALL_CTAS
+#define QKV_DECODE_SMALL_CTAS 2
+#endif
+#ifndef QKV_DECODE_SMALL_SMEM_KB
+#define QKV_DECODE_SMALL_SMEM_KB 110
+#endif
+constexpr int kGroupsLarge = QKV_DECODE_LARGE_GROUPS;
+constexpr int kGroupsSmall = QKV_DECODE_SMALL_GROUPS;
 constexpr size_t kSmallRowBytes = 8192;
 
 #ifndef QKV_DECODE_PAIRS
@@ -348,31 +370,33 @@ struct Unit {
     int off;  // block B starts at row r + off
 };
 
+template <int P = kPairs>
 __device__ __forceinline__ Unit unit_info(int u, int nqt, int nkt, int hd) {
     const int half = hd >> 1;
-    const int per_head = (half + kPairs - 1) / kPairs;
+    const int per_head = (half + P - 1) / P;
     const int uq = (nqt / hd) * per_head, uk = (nkt / hd) * per_head;
     Unit t;
     if (u < uq + uk) {
         t.sec = (u < uq) ? 0 : 1;
         const int v = t.sec ? u - uq : u;
         const int h = v / per_head;
-        const int d0 = (v - h * per_head) * kPairs;
-        t.n = min(kPairs, half - d0);
+        const int d0 = (v - h * per_head) * P;
+        t.n = min(P, half - d0);
         t.r = h * hd + d0;
         t.off = half;
     } else {
         t.sec = 2;
-        t.r = (u - uq - uk) * 2 * kPairs;
-        t.n = min(kPairs, (nkt - t.r) >> 1);
+        t.r = (u - uq - uk) * 2 * P;
+        t.n = min(P, (nkt - t.r) >> 1);
         t.off = t.n;
     }
     return t;
 }
 
+template <int P = kPairs>
 __host__ __device__ __forceinline__ int unit_count(int nqt, int nkt, int hd) {
-    const int per_head = ((hd >> 1) + kPairs - 1) / kPairs;
-    return (nqt / hd) * per_head + (nkt / hd) * per_head + (nkt + 2 * kPairs - 1) / (2 * kPairs);
+    const int per_head = ((hd >> 1) + P - 1) / P;
+    return (nqt / hd) * per_head + (nkt / hd) * per_head + (nkt + 2 * P - 1) / (2 * P);
 }
 
 __device__ __forceinline__ uint4 ld_shared_v4(const void* p) {
@@ -576,6 +600,172 @@ __global__ void __launch_bounds__((kGroups * kGroupWarps + 1) * 32, 2)
     }
 }
 
+// ---------------------------------------------------------------- block ring
+
+#ifndef QKV_DECODE_BLOCK_PAIRS
+#define QKV_DECODE_BLOCK_PAIRS 2
+#endif
+constexpr int kBlkPairs = QKV_DECODE_BLOCK_PAIRS;  // rows per stage (one contiguous bulk copy)
+
+// Block ring: a unit of kBlkPairs neox pairs has two row blocks, (h*hd + d0 ..)
+// and (h*hd + hd/2 + d0 ..); each block is one stage, filled by one contiguous
+// bulk copy.  Item i of a CTA is block (i & 1) of its unit i >> 1 (a contiguous
+// share of all units).  Consumer groups (one warp each) own stages g, g + NG, ...
+// The consumer of a q/k block publishes its biased dot products in shared
+// memory and bumps the unit's counter; the second of the two blocks to finish
+// rotates the unit's pairs and stores them, one pair per lane.  v blocks need
+// no partner and finish on their own.  Each row is reduced exactly as in the
+// pair ring (dot2_staged), so both kernels give the same bits.
+template <typename WT, int MODE, int kGroups>
+__global__ void __launch_bounds__((kGroups + 1) * 32, 1)
+    qkv_decode_blk_kernel(const __grid_constant__ DecodeParams p, int stages, uint32_t stage_bytes,
+                          uint32_t x_bytes, int max_units) {
+    static_assert(kBlkPairs >= 1 && kBlkPairs <= 8, "rows per block");
+    static_assert(kGroupWarps == 1, "one warp per consumer group");
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ float freq_s[QKV_MAX_HEAD_DIM / 2];
+    float4* xs4 = reinterpret_cast<float4*>(smem);
+    unsigned char* ring = smem + x_bytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + static_cast<size_t>(stages) * stage_bytes);
+    uint64_t* empty = full + stages;
+    float* bias_s = reinterpret_cast<float*>(empty + stages);            // [max_units][2][kBlkPairs]
+    float* res = bias_s + max_units * 2 * kBlkPairs;                     // [max_units][2][kBlkPairs]
+    int* cnt = reinterpret_cast<int*>(res + max_units * 2 * kBlkPairs);  // [max_units]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int units = unit_count<kBlkPairs>(p.nqt, p.nkt, p.hd);
+    const int u_begin = static_cast<int>(static_cast<long long>(units) * blockIdx.x / gridDim.x);
+    const int u_end = static_cast<int>(static_cast<long long>(units) * (blockIdx.x + 1) / gridDim.x);
+    const int n = 2 * (u_end - u_begin);
+    const uint32_t row_bytes = static_cast<uint32_t>(p.H) * sizeof(WT);
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < stages; ++st) {
+            mbar_init(&full[st], 1);
+            mbar_init(&empty[st], 1);
+        }
+        mbar_fence_init();
+    }
+    for (int i = threadIdx.x; i < max_units; i += blockDim.x) cnt[i] = 0;
+    __syncthreads();
+    // The next layer's grid may be scheduled now: it reads and writes nothing of
+    // ours before its own griddepcontrol.wait, which waits for this grid to finish.
+    griddep_launch_dependents();
+
+    if (warp == kGroups) {
+        // ---- producer: one lane issues all bulk copies of this CTA ----
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_first();
+            int issued = 0;
+            for (int i = 0; i < n; ++i) {
+                const int st = i % stages;
+                if (i >= stages && !mbar_wait_bounded(&empty[st], ((i / stages) - 1) & 1)) {
+                    flag_timeout();
+                    break;
+                }
+                const Unit t = unit_info<kBlkPairs>(u_begin + (i >> 1), p.nqt, p.nkt, p.hd);
+                const int rb = (i & 1) ? t.r + t.off : t.r;
+                const uint32_t bytes = static_cast<uint32_t>(t.n) * row_bytes;
+                const unsigned char* w = static_cast<const unsigned char*>(p.w[t.sec]);
+                mbar_arrive_expect_tx(&full[st], bytes);
+                bulk_g2s(ring + static_cast<size_t>(st) * stage_bytes, w + static_cast<size_t>(rb) * row_bytes,
+                         bytes, &full[st], pol);
+                ++issued;
+            }
+            // Drain: no copy may still be landing in shared memory when the CTA exits.
+            const int first = issued > stages ? issued - stages : 0;
+            for (int i = first; i < issued; ++i)
+                if (!mbar_wait_bounded(&full[i % stages], (i / stages) & 1)) flag_timeout();
+        }
+        return;
+    }
+
+    // ---- consumers ----
+    // Biases are parameters, not outputs of an earlier kernel: stage this CTA's
+    // share before the dependency wait, so no global load sits in the item loop.
+    if (MODE == kFused) {
+        const int nb = (u_end - u_begin) * 2 * kBlkPairs;
+        for (int e = threadIdx.x; e < nb; e += kGroups * 32) {
+            const int j = e % kBlkPairs, blk = (e / kBlkPairs) & 1, ul = e / (2 * kBlkPairs);
+            const Unit t = unit_info<kBlkPairs>(u_begin + ul, p.nqt, p.nkt, p.hd);
+            bias_s[e] = j < t.n ? __ldg(p.bias[t.sec] + (blk ? t.r + t.off : t.r) + j) : 0.f;
+        }
+    }
+    griddep_wait();
+    {
+        constexpr bool kBf16 = sizeof(WT) == 2;
+        const int nch = p.H / (kBf16 ? 8 : 4);
+        const int tid = threadIdx.x, nthr = kGroups * 32;
+        const float4* xg = reinterpret_cast<const float4*>(p.x);
+        if constexpr (kBf16) {
+            for (int c = tid; c < nch; c += nthr) {
+                xs4[c] = xg[2 * c];
+                xs4[nch + c] = xg[2 * c + 1];
+            }
+        } else {
+            for (int c = tid; c < nch; c += nthr) xs4[c] = xg[c];
+        }
+        for (int i = tid; i < (p.hd >> 1); i += nthr) freq_s[i] = p.inv_freq[i];
+    }
+    named_barrier_sync(1, kGroups * 32);
+    const int pos = (MODE == kFused) ? *p.pos : 0;
+    const bool store = pos_ok(pos, p.n_ctx);
+    if (MODE == kFused && !store && blockIdx.x == 0 && threadIdx.x == 0) flag_bad_pos(pos);
+
+    for (int i = warp; i < n; i += kGroups) {
+        const int st = i % stages;
+        if (!mbar_wait_bounded(&full[st], (i / stages) & 1)) {
+            if (lane == 0) flag_timeout();
+            break;
+        }
+        const int ul = i >> 1, blk = i & 1;
+        const Unit t = unit_info<kBlkPairs>(u_begin + ul, p.nqt, p.nkt, p.hd);
+        const int rb = blk ? t.r + t.off : t.r;
+        const unsigned char* sp = ring + static_cast<size_t>(st) * stage_bytes;
+        float y[kBlkPairs];
+#pragma unroll
+        for (int j = 0; j < kBlkPairs; j += 2) {
+            // rows rb + j and rb + j + 1 (the second repeats the first past the block's end)
+            const int j1 = (j + 1 < t.n) ? j + 1 : j;
+            float a0 = 0.f, a1 = 0.f;
+            if (j < t.n) dot2_staged<WT>(sp + j * row_bytes, sp + j1 * row_bytes, xs4, p.H, lane, a0, a1);
+            y[j] = a0;
+            if (j + 1 < kBlkPairs) y[j + 1] = a1;
+        }
+        __syncwarp();  // every lane is done reading the stage
+        if (lane == 0) mbar_arrive(&empty[st]);
+        // Epilogue: lane j < t.n takes row rb + j of the block.
+        float yl = y[0];
+#pragma unroll
+        for (int j = 1; j < kBlkPairs; ++j)
+            if (lane == j) yl = y[j];
+        const int e = (ul * 2 + blk) * kBlkPairs + lane;
+        if constexpr (MODE == kProjectOnly) {
+            if (lane < t.n) p.out[t.sec][rb + lane] = yl;
+        } else if (t.sec == 2) {
+            if (lane < t.n) epi_v_elem_b(p, rb + lane, yl, bias_s[e], pos, store);
+        } else {
+            const float yb = lane < t.n ? __fadd_rn(yl, bias_s[e]) : 0.f;
+            if (lane < t.n) res[e] = yb;
+            __syncwarp();
+            int first = 0;
+            if (lane == 0) {
+                __threadfence_block();
+                first = atomicAdd(&cnt[ul], 1);
+                __threadfence_block();
+            }
+            first = __shfl_sync(0xffffffffu, first, 0);
+            __syncwarp();
+            if (first == 1 && lane < t.n) {
+                // the partner block is complete: rotate the unit's pair lane
+                const float o = static_cast<volatile float*>(res)[e + (blk ? -kBlkPairs : kBlkPairs)];
+                const int r0 = t.r + lane;
+                epi_qk_rot(p, t.sec, r0, r0 + t.off, blk ? o : yb, blk ? yb : o, pos, freq_s[r0 % p.hd], store);
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------- standalone epilogue
 
 // One thread per unit of the flat index: q pairs, then k pairs, then v elements.
@@ -677,14 +867,14 @@ struct RingShape {
     uint32_t stage_bytes, x_bytes;
 };
 
-// Ring for this layer, or stages = 0 when the shape needs the register-streaming
-// kernel (unaligned rows, or rows too long to stage).  Dynamic shared memory:
-// 225 KB for one CTA per SM, 110 KB each for two.
+// Ring for this layer in a dynamic shared-memory budget, or stages = 0 when the
+// shape needs the register-streaming kernel (unaligned rows, or rows too long to
+// stage).
 template <typename WT>
-RingShape ring_shape(const DecodeParams& p, int groups, int ctas_per_sm) {
+RingShape ring_shape(const DecodeParams& p, int groups, int ctas_per_sm, int smem_kb) {
     RingShape r = {};
     const size_t row = static_cast<size_t>(p.H) * sizeof(WT);
-    const size_t budget = ctas_per_sm == 1 ? 225 * 1024 : 110 * 1024;
+    const size_t budget = static_cast<size_t>(smem_kb) * 1024;
     r.ctas_per_sm = ctas_per_sm;
     r.stage_bytes = static_cast<uint32_t>((2 * kPairs * row + 127) / 128 * 128);
     r.x_bytes = static_cast<uint32_t>((static_cast<size_t>(p.H) * 4 + 127) / 128 * 128);
@@ -720,15 +910,61 @@ cudaError_t launch_decode_tma(const DecodeParams& p, const RingShape& r, bool pd
     return cudaLaunchKernelEx(&cfg, kernel, p, r.stages, r.stage_bytes, r.x_bytes);
 }
 
+
+// Block ring in a dynamic shared-memory budget (0 stages: does not fit).
+template <typename WT, int MODE, int kGroups>
+cudaError_t launch_decode_blk(const DecodeParams& p, int ctas_per_sm, int smem_kb, bool pdl, cudaStream_t stream,
+                              bool& launched) {
+    launched = false;
+    const size_t row = static_cast<size_t>(p.H) * sizeof(WT);
+    const uint32_t stage_bytes = static_cast<uint32_t>((kBlkPairs * row + 127) / 128 * 128);
+    const uint32_t x_bytes = static_cast<uint32_t>((static_cast<size_t>(p.H) * 4 + 127) / 128 * 128);
+    const int units = unit_count<kBlkPairs>(p.nqt, p.nkt, p.hd);
+    const int ctas_max = sm_count() * ctas_per_sm;
+    const int grid = units < ctas_max ? units : ctas_max;
+    const int max_units = (units + grid - 1) / grid;
+    // per unit: staged biases, published results and a counter
+    const size_t tail = static_cast<size_t>(max_units) * (4 * kBlkPairs * sizeof(float) + sizeof(int));
+    const size_t budget = static_cast<size_t>(smem_kb) * 1024;
+    const size_t fixed = x_bytes + tail + 2 * 32 * sizeof(uint64_t);
+    if (fixed + static_cast<size_t>(kGroups) * stage_bytes > budget) return cudaSuccess;
+    int stages = static_cast<int>((budget - fixed) / stage_bytes);
+    stages = stages > kMaxStages ? kMaxStages : stages;
+    stages -= stages % kGroups;
+    auto kernel = qkv_decode_blk_kernel<WT, MODE, kGroups>;
+    const size_t smem = x_bytes + static_cast<size_t>(stages) * stage_bytes + 2 * stages * sizeof(uint64_t) + tail;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3((kGroups + 1) * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    launched = true;
+    return cudaLaunchKernelEx(&cfg, kernel, p, stages, stage_bytes, x_bytes, max_units);
+}
+
 template <typename WT, bool VEC, int MODE>
 cudaError_t launch_decode_t(const DecodeParams& p, bool pdl, cudaStream_t stream) {
     if constexpr (VEC) {
         const size_t row = static_cast<size_t>(p.H) * sizeof(WT);
         if (row >= kSmallRowBytes) {
-            const RingShape r = ring_shape<WT>(p, kGroupsLarge, 1);
+            // rows of >= 8 KB: block ring (one contiguous copy per stage), else the pair ring
+            bool launched = false;
+            const cudaError_t e = launch_decode_blk<WT, MODE, kGroupsLarge>(p, QKV_DECODE_LARGE_CTAS,
+                                                                             QKV_DECODE_LARGE_SMEM_KB, pdl, stream,
+                                                                             launched);
+            if (launched || e != cudaSuccess) return e;
+            const RingShape r = ring_shape<WT>(p, kGroupsLarge, QKV_DECODE_LARGE_CTAS, QKV_DECODE_LARGE_SMEM_KB);
             if (r.stages > 0) return launch_decode_tma<WT, MODE, kGroupsLarge>(p, r, pdl, stream);
         } else {
-            const RingShape r = ring_shape<WT>(p, kGroupsSmall, 2);
+            const RingShape r = ring_shape<WT>(p, kGroupsSmall, QKV_DECODE_SMALL_CTAS, QKV_DECODE_SMALL_SMEM_KB);
             if (r.stages > 0) return launch_decode_tma<WT, MODE, kGroupsSmall>(p, r, pdl, stream);
         }
     }

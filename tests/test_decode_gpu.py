@@ -82,6 +82,9 @@ SHAPES = [
     (5120, 40, 8, 128, "bf16", "f16", 4096, 3254),  # Qwen2.5-14B layer
     (256, 64, 8, 128, "bf16", "f16", 64, 33),  # 5120 row pairs, 16-stage ring wraps twice per CTA
     (1024, 96, 16, 64, "f32", "f32", 40, 39),  # f32 rows, 4 KB stages, ring wraps per CTA
+    (2048, 8, 2, 128, "f32", "f16", 64, 20),   # f32 rows of 8 KB: block ring
+    (4096, 64, 8, 128, "bf16", "f32", 16, 15),  # block ring wraps several times per CTA
+    (4096, 3, 1, 2, "bf16", "f16", 4, 2),      # hd = 2: single-row blocks
 ]
 
 
