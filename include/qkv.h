@@ -196,8 +196,10 @@ qkv_status qkv_chain_store(const qkv_plan* plan, const float* src, void* cache,
  *   X           device, nt x H bf16 (row-major).
  *   d_positions device, nt int32, distinct positions.
  *   Y           device, nt x R floats: per token q | k | v after the epilogue.
- * Errors: INVALID_ARG, UNSUPPORTED (f32 weights, mixed class, H % 64 != 0),
- * CUDA. */
+ * X, w, Y, kv_k and kv_v must be 16-byte aligned (TMA operands and 16-byte
+ * cache stores).
+ * Errors: INVALID_ARG (null or misaligned pointers), UNSUPPORTED (f32
+ * weights, mixed class, head_dim % 64 != 0, hidden % 8 != 0), CUDA. */
 qkv_status qkv_prefill_step(const qkv_plan* plan, const uint16_t* X, int32_t nt,
                             const void* w, const float* bias, const int32_t* d_positions,
                             float* Y, void* kv_k, void* kv_v, void* stream);

@@ -12,13 +12,22 @@
 // (UMMA N).  The 64 rows are two 32-row boxes chosen so that every neox pair
 // lands in one thread: for a q or k tile, rows (h*hd + d0 .. +31) and
 // (h*hd + hd/2 + d0 .. +31); for a v tile, 64 consecutive rows.  K advances in
-// blocks of 64 bf16 (128 bytes, one 128B-swizzle row).  Warp 0 lane 0 loads
-// X and W tiles with TMA into a 6-stage ring (mbarrier transaction counts);
+// blocks of 64 bf16 (128 bytes, one 128B-swizzle row).  CTAs of a thread-block
+// cluster (CN consecutive row tiles, same tokens) share X: each loads a 1/CN
+// slice of every X stage with TMA multicast, so one L2 read feeds CN CTAs.
+// Warp 0 lane 0 streams W boxes into a 6-stage ring (before the dependency wait:
+// weights are parameters) and warp 2 lane 0 its X slices into a 4-stage ring
+// (mbarrier transaction counts; an X stage is reused once all CN CTAs of the
+// cluster released it);
 // warp 1 lane 0 issues tcgen05.mma (kind::f16, bf16 x bf16 -> f32 in TMEM,
-// 4 MMAs of K = 16 per stage) and frees each stage with tcgen05.commit; then
+// 4 MMAs of K = 16 per block) and releases each stage in every CTA of the cluster
+// with a multicast tcgen05.commit; then
 // all four warps read their 32 TMEM lanes (one token each) with tcgen05.ld and
-// run the epilogue.  Every wait is bounded; on expiry the kernel flags the
-// device status word, drains in-flight copies and MMAs, frees TMEM and returns.
+// run the epilogue: Y leaves through shared memory (128-byte swizzle) and two
+// TMA tensor stores, the token's k/v cache rows as 16-byte stores.  Every wait
+// is bounded; on expiry the kernel flags the device status word, drains
+// in-flight copies and MMAs, frees TMEM and returns.  A CTA leaves only after a
+// cluster barrier, so no peer still writes into it.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -39,13 +48,19 @@ constexpr int kUK = 16;                        // K per tcgen05.mma, kind::f16
 #ifndef QKV_PREFILL_KSUB
 #define QKV_PREFILL_KSUB 2
 #endif
-#ifndef QKV_PREFILL_STAGES
-#define QKV_PREFILL_STAGES 4
+#ifndef QKV_PREFILL_X_STAGES
+#define QKV_PREFILL_X_STAGES 4
+#endif
+#ifndef QKV_PREFILL_W_STAGES
+#define QKV_PREFILL_W_STAGES 6
 #endif
 // A stage holds kSub consecutive 64-wide K blocks, so each weight row is
-// requested kSub * 128 contiguous bytes at a time.
+// requested kSub * 128 contiguous bytes at a time.  X (L2-resident, shared by
+// the cluster) and W (streamed from HBM) have rings of their own: W, the long-
+// latency stream, gets the deeper one.
 constexpr int kSub = QKV_PREFILL_KSUB;
-constexpr int kStages = QKV_PREFILL_STAGES;
+constexpr int kXStages = QKV_PREFILL_X_STAGES;
+constexpr int kWStages = QKV_PREFILL_W_STAGES;
 constexpr int kThreads = 128;
 constexpr uint32_t kABlk = kBM * kBK * 2;      // 16 KB: one X block (128 x 64)
 constexpr uint32_t kBBlk = kBN * kBK * 2;      // 8 KB: one W block (64 x 64)
@@ -53,8 +68,9 @@ constexpr uint32_t kABytes = kSub * kABlk;     // X bytes per stage
 constexpr uint32_t kBBytes = kSub * kBBlk;     // W bytes per stage
 constexpr uint32_t kBoxBytes = kBox * kBK * 2; // 4 KB
 constexpr uint32_t kTmemCols = 64;             // f32 accumulator columns (= kBN)
-constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStages * (kABytes + kBBytes) +
-                              (2 * kStages + 1) * sizeof(uint64_t) + 16;
+constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kXStages * kABytes + kWStages * kBBytes +
+                              (2 * kXStages + 2 * kWStages + 1) * sizeof(uint64_t) + 16;
+static_assert(kSmemBytes <= 227 * 1024, "prefill rings exceed shared memory");
 
 constexpr unsigned int kFlagPosRange = 1u;
 constexpr unsigned int kFlagTimeout = 2u;
@@ -76,6 +92,61 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
         : "memory");
+}
+
+// The same box into the same shared-memory offset of every CTA in `mask`; each
+// destination CTA's barrier at `bar`'s offset receives the bytes it got.
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar,
+                                               uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(mask)
+        : "memory");
+}
+
+// Shared -> global tensor store of one box (rows past the tensor's extent are
+// not written); completion tracked by this thread's bulk async-group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(smem_u32(src))
+                 : "memory");
+}
+
+// Commit this thread's bulk stores and wait until their shared-memory sources
+// have been read (the global writes complete on their own before the grid does).
+__device__ __forceinline__ void bulk_commit_and_wait_read() {
+    asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Generic-proxy writes to shared memory become visible to the async proxy (TMA).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_count_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+// All threads of every CTA in the cluster; release/acquire orders shared-memory
+// state (barrier initialisation) across the cluster.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
@@ -129,6 +200,16 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
                  : "memory");
 }
 
+// Arrive once on the barrier at `bar`'s offset in every CTA of `mask` when the
+// MMAs issued so far have completed.
+__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(mask)
+        : "memory");
+}
+
 // 32 consecutive f32 columns of this warp's 32 TMEM lanes: thread l gets lane
 // (warp's base lane + l), columns col .. col + 31.
 __device__ __forceinline__ void tc_ld_32cols(uint32_t taddr, float* v) {
@@ -153,18 +234,20 @@ __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sy
 
 __global__ void __launch_bounds__(kThreads, 1)
     qkv_prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-                       const __grid_constant__ PrefillParams p) {
+                       const __grid_constant__ CUtensorMap tm_y, const __grid_constant__ PrefillParams p, int cn) {
     extern __shared__ unsigned char smem_raw[];
     __shared__ float bias_s[kBN];
     __shared__ float freq_s[kBox];
     __shared__ uint32_t tmem_slot;
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    unsigned char* sA = smem;
-    unsigned char* sB = smem + kStages * kABytes;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
-    uint64_t* empty = full + kStages;
-    uint64_t* done = empty + kStages;
+    unsigned char* sA = smem;                          // X ring
+    unsigned char* sB = smem + kXStages * kABytes;     // W ring
+    uint64_t* xfull = reinterpret_cast<uint64_t*>(sB + kWStages * kBBytes);
+    uint64_t* xempty = xfull + kXStages;
+    uint64_t* wfull = xempty + kXStages;
+    uint64_t* wempty = wfull + kWStages;
+    uint64_t* done = wempty + kWStages;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.y * kBM;
@@ -188,12 +271,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int base = sec == 0 ? 0 : (sec == 1 ? p.nqt : p.nqt + p.nkt);  // section's first global row
     const int nk = (p.H + kSub * kBK - 1) / (kSub * kBK);  // stages of kSub K blocks
-    // CTAs start their K loop at different blocks, so the X tiles they read at
-    // any moment are spread over L2 instead of every CTA hitting the same lines.
+    // Clusters start their K loop at different blocks, so the X tiles read at any
+    // moment are spread over L2; the CTAs of one cluster share X and move together.
 #ifndef QKV_PREFILL_STAGGER
 #define QKV_PREFILL_STAGGER 1
 #endif
-    const int k_first = QKV_PREFILL_STAGGER ? static_cast<int>((static_cast<long long>(tile) * nk) / gridDim.x) : 0;
+    const int k_first =
+        QKV_PREFILL_STAGGER ? static_cast<int>((static_cast<long long>(cluster_id_x()) * nk) / cluster_count_x()) : 0;
+    const uint32_t rank = cluster_rank();
+    const uint16_t cmask = static_cast<uint16_t>((1u << cn) - 1u);
+    const int slice = kBM / cn;  // X rows this CTA loads (and multicasts) per block
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -203,9 +290,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (threadIdx.x == 32) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+        for (int s = 0; s < kXStages; ++s) {
+            mbar_init(&xfull[s], 1);
+            mbar_init(&xempty[s], static_cast<uint32_t>(cn));  // one release from each CTA of the cluster
+        }
+        for (int s = 0; s < kWStages; ++s) {
+            mbar_init(&wfull[s], 1);
+            mbar_init(&wempty[s], 1);
         }
         mbar_init(done, 1);
         mbar_fence_init();
@@ -214,63 +305,102 @@ __global__ void __launch_bounds__(kThreads, 1)
     else if (threadIdx.x < 2 * kBox) bias_s[threadIdx.x] = p.bias[base + rowB + threadIdx.x - kBox];
     else if (threadIdx.x < 3 * kBox && sec < 2) freq_s[threadIdx.x - 2 * kBox] = p.inv_freq[d0 + threadIdx.x - 2 * kBox];
     tc_fence_before();
-    __syncthreads();
+    // every barrier of the cluster is initialised before any peer copies or commits to it
+    cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
-    // X, positions and the outputs may belong to the preceding grid in the
-    // stream: wait for it before any of them is touched; the next grid may be
-    // scheduled now (it waits for this one in the same way).
-    griddep_wait();
+    // The next grid may be scheduled now (it waits for this one before it reads
+    // anything this one writes).  X, positions and the outputs may belong to the
+    // preceding grid in the stream: every thread waits for it before touching
+    // them.  Weights are parameters, so the W producer streams them first.
     griddep_launch_dependents();
+    if (!(warp == 0 && lane == 0)) griddep_wait();
 
     if (warp == 0 && lane == 0) {
-        // ---- producer: TMA tiles of X (128 x 64) and W (two 32 x 64 boxes) per stage ----
-        prefetch_tensormap(&tm_x);
+        // ---- W producer: two 32 x 64 boxes per K block, local ring ----
         prefetch_tensormap(&tm_w);
         int issued = 0;
         for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % kStages;
-            if (kb >= kStages && !mbar_wait_bounded(&empty[s], ((kb / kStages) - 1) & 1)) {
+            const int s = kb % kWStages;
+            if (kb >= kWStages && !mbar_wait_bounded(&wempty[s], ((kb / kWStages) - 1) & 1)) {
                 flag_timeout();
                 break;
             }
             const int kx = (k_first + kb) % nk;  // stage index along K
-            mbar_arrive_expect_tx(&full[s], kABytes + kBBytes);
+            mbar_arrive_expect_tx(&wfull[s], kBBytes);
 #pragma unroll
             for (int j = 0; j < kSub; ++j) {
                 const int kc = (kx * kSub + j) * kBK;  // element column of this 64-wide block
                 unsigned char* b = sB + s * kBBytes + j * kBBlk;
-                tma_load_2d(b, &tm_w, kc, base + rowA, &full[s]);
-                tma_load_2d(b + kBoxBytes, &tm_w, kc, base + rowB, &full[s]);
+                tma_load_2d(b, &tm_w, kc, base + rowA, &wfull[s]);
+                tma_load_2d(b + kBoxBytes, &tm_w, kc, base + rowB, &wfull[s]);
             }
-#pragma unroll
-            for (int j = 0; j < kSub; ++j)
-                tma_load_2d(sA + s * kABytes + j * kABlk, &tm_x, (kx * kSub + j) * kBK, m0, &full[s]);
             ++issued;
         }
-        // Drain: no copy may still be landing in shared memory when the CTA exits.
-        const int first = issued > kStages ? issued - kStages : 0;
-        for (int kb = first; kb < issued; ++kb)
-            if (!mbar_wait_bounded(&full[kb % kStages], (kb / kStages) & 1)) flag_timeout();
+        // Drain: every W copy has landed and the MMAs released the last stages.
+        const int first = issued > kWStages ? issued - kWStages : 0;
+        for (int kb = first; kb < issued; ++kb) {
+            if (!mbar_wait_bounded(&wfull[kb % kWStages], (kb / kWStages) & 1)) flag_timeout();
+            if (!mbar_wait_bounded(&wempty[kb % kWStages], (kb / kWStages) & 1)) flag_timeout();
+        }
+        griddep_wait();  // before this thread writes its epilogue rows
+    } else if (warp == 2 && lane == 0) {
+        // ---- X producer: this CTA's slice of each 128 x 64 X block, multicast to the cluster ----
+        prefetch_tensormap(&tm_x);
+        int issued = 0;
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % kXStages;
+            if (kb >= kXStages && !mbar_wait_bounded(&xempty[s], ((kb / kXStages) - 1) & 1)) {
+                flag_timeout();
+                break;
+            }
+            const int kx = (k_first + kb) % nk;
+            mbar_arrive_expect_tx(&xfull[s], kABytes);  // the whole block: every CTA's slice lands here
+#pragma unroll
+            for (int j = 0; j < kSub; ++j) {
+                unsigned char* a = sA + s * kABytes + j * kABlk + static_cast<uint32_t>(rank) * slice * (kBK * 2);
+                const int kc = (kx * kSub + j) * kBK;
+                if (cn == 1)
+                    tma_load_2d(a, &tm_x, kc, m0, &xfull[s]);
+                else
+                    tma_load_2d_mc(a, &tm_x, kc, m0 + static_cast<int>(rank) * slice, &xfull[s], cmask);
+            }
+            ++issued;
+        }
+        // Drain: every slice into this CTA (its own and its peers') has landed, and
+        // every CTA of the cluster released the last stages, so no peer commit is
+        // still on its way to these barriers.
+        const int first = issued > kXStages ? issued - kXStages : 0;
+        for (int kb = first; kb < issued; ++kb) {
+            if (!mbar_wait_bounded(&xfull[kb % kXStages], (kb / kXStages) & 1)) flag_timeout();
+            if (!mbar_wait_bounded(&xempty[kb % kXStages], (kb / kXStages) & 1)) flag_timeout();
+        }
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer ----
         for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % kStages;
-            if (!mbar_wait_bounded(&full[s], (kb / kStages) & 1)) {
+            const int xs = kb % kXStages, ws = kb % kWStages;
+            if (!mbar_wait_bounded(&xfull[xs], (kb / kXStages) & 1) ||
+                !mbar_wait_bounded(&wfull[ws], (kb / kWStages) & 1)) {
                 flag_timeout();
                 break;
             }
             tc_fence_after();
 #pragma unroll
             for (int j = 0; j < kSub; ++j) {
-                const unsigned char* a = sA + s * kABytes + j * kABlk;
-                const unsigned char* b = sB + s * kBBytes + j * kBBlk;
+                const unsigned char* a = sA + xs * kABytes + j * kABlk;
+                const unsigned char* b = sB + ws * kBBytes + j * kBBlk;
 #pragma unroll
                 for (int k = 0; k < kBK / kUK; ++k)
                     tc_mma(tmem, smem_desc_k128(a + k * kUK * 2), smem_desc_k128(b + k * kUK * 2),
                            (kb | j | k) != 0);
             }
-            tc_commit(&empty[s]);  // the stage is free once these MMAs have read it
+            // Both stages are free in this CTA once these MMAs have read them; an X
+            // stage must be freed by every CTA of the cluster before a peer reloads it.
+            tc_commit(&wempty[ws]);
+            if (cn == 1)
+                tc_commit(&xempty[xs]);
+            else
+                tc_commit_mc(&xempty[xs], cmask);
         }
         tc_commit(done);  // arrives when every MMA issued above has completed
     }
@@ -288,14 +418,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_ld_32cols(taddr + kBox, acc + kBox);
         tc_wait_ld();
     }
-    const int t = m0 + warp * 32 + lane;
-    if (acc_ready && t < p.nt) {
-        const int pos = p.positions[t];
-        const bool store = pos_ok(pos, p.n_ctx);
-        if (!store) flag_bad_pos(pos);
-        const int R = p.nqt + 2 * p.nkt;
-        float* yrow = p.Y + static_cast<size_t>(t) * R + base;
-        const size_t kvrow = static_cast<size_t>(store ? pos : 0) * static_cast<size_t>(p.nkt);
+    const int tl = warp * 32 + lane;  // this thread's token within the tile
+    const int t = m0 + tl;
+    if (acc_ready) {
+        const bool live = t < p.nt;
+        const int pos = live ? p.positions[t] : 0;
+        const bool store = live && pos_ok(pos, p.n_ctx);
+        if (live && !store) flag_bad_pos(pos);
         if (sec < 2) {
 #pragma unroll
             for (int i = 0; i < kBox; ++i) {
@@ -310,23 +439,63 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < kBN; ++i) acc[i] = __fadd_rn(acc[i], bias_s[i]);
         }
+        // Y: stage both 32-column boxes in the (now idle) ring, row tl of each box,
+        // in the 128-byte-swizzled layout the Y tensor map stores from.
+        float* ys = reinterpret_cast<float*>(smem);
 #pragma unroll
-        for (int i = 0; i < kBox; i += 4) {
-            *reinterpret_cast<float4*>(yrow + rowA + i) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
-            *reinterpret_cast<float4*>(yrow + rowB + i) =
-                make_float4(acc[kBox + i], acc[kBox + i + 1], acc[kBox + i + 2], acc[kBox + i + 3]);
+        for (int c = 0; c < kBox / 4; ++c) {
+            const int sw = (c ^ (tl & 7)) * 4;
+            *reinterpret_cast<float4*>(ys + tl * kBox + sw) =
+                make_float4(acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
+            *reinterpret_cast<float4*>(ys + kBM * kBox + tl * kBox + sw) =
+                make_float4(acc[kBox + 4 * c], acc[kBox + 4 * c + 1], acc[kBox + 4 * c + 2], acc[kBox + 4 * c + 3]);
         }
+        // k and v rows of the cache: 16-byte stores of this token's two 32-column runs.
         if (store && sec > 0) {
+            const size_t kvrow = static_cast<size_t>(pos) * static_cast<size_t>(p.nkt);
             void* kv = sec == 1 ? p.kv_k : p.kv_v;
+            if (p.kv_f16) {
+                __half* dst = static_cast<__half*>(kv) + kvrow;
 #pragma unroll
-            for (int i = 0; i < kBox; ++i) {
-                kv_put(kv, p.kv_f16, kvrow + rowA + i, acc[i]);
-                kv_put(kv, p.kv_f16, kvrow + rowB + i, acc[kBox + i]);
+                for (int c = 0; c < kBox / 8; ++c) {
+                    uint4 ua, ub;
+                    uint32_t* pa = &ua.x;
+                    uint32_t* pb = &ub.x;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        pa[e] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc[8 * c + 2 * e]))) |
+                                (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc[8 * c + 2 * e + 1]))) << 16);
+                        pb[e] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc[kBox + 8 * c + 2 * e]))) |
+                                (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc[kBox + 8 * c + 2 * e + 1])))
+                                 << 16);
+                    }
+                    *reinterpret_cast<uint4*>(dst + rowA + 8 * c) = ua;
+                    *reinterpret_cast<uint4*>(dst + rowB + 8 * c) = ub;
+                }
+            } else {
+                float* dst = static_cast<float*>(kv) + kvrow;
+#pragma unroll
+                for (int c = 0; c < kBox / 4; ++c) {
+                    *reinterpret_cast<float4*>(dst + rowA + 4 * c) =
+                        make_float4(acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
+                    *reinterpret_cast<float4*>(dst + rowB + 4 * c) = make_float4(
+                        acc[kBox + 4 * c], acc[kBox + 4 * c + 1], acc[kBox + 4 * c + 2], acc[kBox + 4 * c + 3]);
+                }
             }
         }
     }
+    fence_proxy_async_smem();
+    // Every warp has staged its rows (or the accumulator never became ready).
+    const bool tile_ready = __syncthreads_and(acc_ready) != 0;
+    if (tile_ready && threadIdx.x == 0) {
+        const float* ys = reinterpret_cast<const float*>(smem);
+        tma_store_2d(&tm_y, ys, base + rowA, m0);
+        tma_store_2d(&tm_y, ys + kBM * kBox, base + rowB, m0);
+        bulk_commit_and_wait_read();  // the boxes are read out before the CTA lets go of its shared memory
+    }
     tc_fence_before();
-    __syncthreads();
+    // No CTA leaves while a peer of its cluster may still write into it.
+    cluster_sync_all();
     if (warp == 0) {
         // After a timeout, give in-flight MMAs a second bounded wait before the
         // accumulator columns are released.
@@ -350,6 +519,20 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
             fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
     }
     return fn;
+}
+
+// 2-D f32 tensor map over a row-major [rows x cols] matrix for stores: box
+// [box_rows x 32] (128-byte rows), 128-byte swizzle; rows past `rows` are not written.
+bool encode_f32_2d_store(CUtensorMap* map, void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 4};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBox), box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // 2-D bf16 tensor map over a row-major [rows x cols] matrix, box [box_rows x 64],
@@ -385,9 +568,22 @@ qkv_status launch_prefill(const PrefillParams& p, bool pdl, cudaStream_t stream,
         *why = "Y must be 16-byte aligned";
         return QKV_ERR_INVALID_ARG;
     }
+    if ((reinterpret_cast<uintptr_t>(p.kv_k) | reinterpret_cast<uintptr_t>(p.kv_v)) & 15) {
+        *why = "the KV regions must be 16-byte aligned";
+        return QKV_ERR_INVALID_ARG;
+    }
     const int R = p.nqt + 2 * p.nkt;
-    CUtensorMap tm_x, tm_w;
-    if (!encode_bf16_2d(&tm_x, p.X, static_cast<uint64_t>(p.nt), static_cast<uint64_t>(p.H), kBM) ||
+    const int tiles = R / kBN;
+    // Cluster of CN consecutive row tiles sharing X: the largest of 4, 2, 1 that divides the tiles.
+#ifndef QKV_PREFILL_CLUSTER
+#define QKV_PREFILL_CLUSTER 4
+#endif
+    int cn = QKV_PREFILL_CLUSTER;
+    while (cn > 1 && tiles % cn != 0) cn >>= 1;
+    CUtensorMap tm_x, tm_w, tm_y;
+    if (!encode_f32_2d_store(&tm_y, p.Y, static_cast<uint64_t>(p.nt), static_cast<uint64_t>(R), kBM) ||
+        !encode_bf16_2d(&tm_x, p.X, static_cast<uint64_t>(p.nt), static_cast<uint64_t>(p.H),
+                        static_cast<uint32_t>(kBM / cn)) ||
         !encode_bf16_2d(&tm_w, p.W, static_cast<uint64_t>(R), static_cast<uint64_t>(p.H), kBox)) {
         *why = "cuTensorMapEncodeTiled failed or is unavailable";
         return QKV_ERR_CUDA;
@@ -399,16 +595,20 @@ qkv_status launch_prefill(const PrefillParams& p, bool pdl, cudaStream_t stream,
         return QKV_ERR_CUDA;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(R / kBN, (p.nt + kBM - 1) / kBM);
+    cfg.gridDim = dim3(tiles, (p.nt + kBM - 1) / kBM);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cn);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, qkv_prefill_kernel, tm_x, tm_w, p);
+    cfg.numAttrs = pdl ? 2 : 1;
+    e = cudaLaunchKernelEx(&cfg, qkv_prefill_kernel, tm_x, tm_w, tm_y, p, cn);
     if (e != cudaSuccess) {
         *why = cudaGetErrorString(e);
         return QKV_ERR_CUDA;

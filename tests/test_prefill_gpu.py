@@ -79,6 +79,8 @@ SHAPES = [
     (130, 1000, 2, 2, 64, 300, "f16"),      # K tail of 40 elements, M tail of 2 tokens
     (128, 1024, 4, 2, 128, 256, "f32"),
     (37, 5120, 40, 8, 128, 4096, "f16"),    # 14B layer shape
+    (3, 256, 3, 1, 64, 8, "f16"),           # 5 row tiles: no cluster sharing
+    (9, 512, 1, 1, 64, 12, "f32"),          # 3 row tiles: no cluster sharing
 ]
 
 
