@@ -65,6 +65,9 @@ def _bind(lib):
     lib.oracle_qkv_prefill.argtypes = [vp, i, vp, i, vp, vp, i, i, i, i, d, d, i, i, vp, vp, vp,
                                        vp, vp]
     lib.oracle_qkv_prefill.restype = i
+    lib.oracle_silu.argtypes = [d]
+    lib.oracle_silu.restype = d
+    lib.oracle_ffn_swiglu.argtypes = [vp, i, vp, i64, i64, vp]
     return lib
 
 
@@ -120,6 +123,19 @@ class Oracle:
         y = np.empty(R, dtype=np.float64)
         self.lib.oracle_matvec(_p(W), int(W.dtype == np.uint16), _p(x), R, H, _p(y))
         return y
+
+    def silu(self, v: float) -> float:
+        return float(self.lib.oracle_silu(float(v)))
+
+    def ffn_swiglu(self, W: np.ndarray, x: np.ndarray) -> np.ndarray:
+        """silu(gate) * up over a concat gate|up weight W [2 nf, H] (float32 or bf16 bits)."""
+        W = np.ascontiguousarray(W)
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        R, H = W.shape
+        assert R % 2 == 0, "the gate|up weight has 2 nf rows"
+        out = np.empty(R // 2, dtype=np.float32)
+        self.lib.oracle_ffn_swiglu(_p(W), int(W.dtype == np.uint16), _p(x), R // 2, H, _p(out))
+        return out
 
     def token(self, y, bias, nh, nkv, hd, base, freq_scale, pos, kv_k, kv_v):
         """Epilogue for one token on a precomputed projection y (float64 [R])."""

@@ -15,7 +15,12 @@
  *     pos * nkt + j, f16 conversion round-to-nearest);
  *   - "07 · The allocator: liveness, buffer reuse, and the KV cache", §2.5
  *     (per-layer K and V regions of n_ctx rows x nkt) and §3.4 (a position
- *     >= n_ctx is an error, never an overflow).
+ *     >= n_ctx is an error, never an overflow);
+ *   - "06 · Assign + fusion — every node picks an engine, then patterns
+ *     fold", §2.2 (the FFN activation: gate and up projections of the normed
+ *     hidden state, SiLU(x) = x * sigmoid(x), then the elementwise product)
+ *     and §2.3 (the decode FusedFFN node: one concat gate|up weight, then the
+ *     SwiGLU over the two halves of its output).
  *
  * Precision: everything is carried in double; results are rounded to f32 (or
  * f32 then f16) only where the stage stores them.  Readings taken where the
@@ -235,4 +240,37 @@ int oracle_qkv_prefill(const uint16_t* X, int nt, const void* W, int w_is_bf16,
         if (s != ORACLE_OK && status == ORACLE_OK) status = s;
     }
     return status;
+}
+
+/* ---- FusedFFN (decode, one token) ----------------------------------------- */
+
+/* SiLU(v) = v * sigmoid(v) = v / (1 + e^-v), in double. */
+double oracle_silu(double v) { return v / (1.0 + exp(-v)); }
+
+/* The concat gate|up projection followed by SwiGLU.
+ *   W      row-major [2 nf x H]: rows 0 .. nf-1 are W_gate, rows nf .. 2nf-1 W_up
+ *          (f32 values, or bf16 bit patterns when w_is_bf16).
+ *   x      the normed hidden state [H].
+ *   out[i] = RN_f32( silu(gate_i) * up_i ),  gate_i = (W x)[i],  up_i = (W x)[nf + i],
+ *          every sum and product in double. */
+void oracle_ffn_swiglu(const void* W, int w_is_bf16, const float* x, int64_t nf, int64_t H, float* out) {
+    for (int64_t i = 0; i < nf; ++i) {
+        double g = 0.0, u = 0.0;
+        if (w_is_bf16) {
+            const uint16_t* rg = (const uint16_t*)W + i * H;
+            const uint16_t* ru = (const uint16_t*)W + (nf + i) * H;
+            for (int64_t c = 0; c < H; ++c) {
+                g += oracle_bf16_value(rg[c]) * (double)x[c];
+                u += oracle_bf16_value(ru[c]) * (double)x[c];
+            }
+        } else {
+            const float* rg = (const float*)W + i * H;
+            const float* ru = (const float*)W + (nf + i) * H;
+            for (int64_t c = 0; c < H; ++c) {
+                g += (double)rg[c] * (double)x[c];
+                u += (double)ru[c] * (double)x[c];
+            }
+        }
+        out[i] = (float)(oracle_silu(g) * u);
+    }
 }

@@ -31,6 +31,7 @@ T_BIAS = 2        # concat bq|bk|bv, keyed by index 0
 T_HIDDEN = 3      # decode hidden vector x, keyed by position
 T_PREFILL_X = 4   # prefill activations X[t], keyed by token index t
 T_CANARY = 5      # KV-cache fill pattern for untouched-slot checks
+T_FFN_WEIGHT = 6  # concat w_gate|w_up rows of the FFN, keyed by global row index
 
 W_SIGMA = 0.02
 BIAS_SIGMA = 0.1
@@ -117,6 +118,12 @@ def weight_rows(seed: int, layer: int, row0: int, nrows: int, hidden: int, dtype
                 out: np.ndarray | None = None) -> np.ndarray:
     """Rows [row0, row0+nrows) of the concatenated wq|wk|wv matrix, ~N(0, 0.02)."""
     return rows(seed, T_WEIGHT, layer, row0, nrows, hidden, W_SIGMA, dtype, out)
+
+
+def ffn_weight_rows(seed: int, layer: int, row0: int, nrows: int, hidden: int, dtype: str,
+                    out: np.ndarray | None = None) -> np.ndarray:
+    """Rows [row0, row0+nrows) of the concatenated w_gate|w_up matrix, ~N(0, 0.02)."""
+    return rows(seed, T_FFN_WEIGHT, layer, row0, nrows, hidden, W_SIGMA, dtype, out)
 
 
 def bias(seed: int, layer: int, n_rows: int) -> np.ndarray:

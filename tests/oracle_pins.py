@@ -399,4 +399,70 @@ def pin_prefill_equals_decode(orc):
     assert np.array_equal(kp, kd) and np.array_equal(vp, vd)
 
 
+# ---------------------------------------------------------------- FusedFFN
+
+def pin_silu_special_values(orc):
+    """SiLU(v) = v * sigmoid(v): SiLU(0) = 0; sigmoid(ln 3) = 3/4, so SiLU(ln 3) = 0.75 ln 3;
+    SiLU(v) - SiLU(-v) = v (since sigmoid(v) + sigmoid(-v) = 1); SiLU(v) -> v for large v
+    and -> v e^v for very negative v; other points against mpmath."""
+    import mpmath
+    mpmath.mp.dps = 50
+    assert orc.silu(0.0) == 0.0
+    ln3 = math.log(3.0)
+    assert abs(orc.silu(ln3) - 0.75 * ln3) <= 1e-15 * ln3
+    for v in (0.125, 1.0, 2.5, 7.0, 19.0):
+        assert abs((orc.silu(v) - orc.silu(-v)) - v) <= 1e-14 * v, v
+    assert abs(orc.silu(40.0) - 40.0) <= 1e-13
+    assert abs(orc.silu(-40.0) - (-40.0 * math.exp(-40.0))) <= 1e-12 * 40.0 * math.exp(-40.0)
+    for v in (-3.75, -0.5, 0.3, 1.7, 6.25):
+        exact = mpmath.mpf(v) / (1 + mpmath.exp(-mpmath.mpf(v)))
+        assert abs(orc.silu(v) - float(exact)) <= 1e-15 * max(1.0, abs(float(exact))), v
+
+
+def _ffn_hand_case():
+    """nf = 3, H = 4, small integers and halves: exact in f32, bf16 and float64.
+    gate_i = sum_c (i - c) x_c and up_i = sum_c (i + 2c + 1) x_c are all distinct."""
+    nf, H = 3, 4
+    i = np.arange(nf)[:, None]
+    c = np.arange(H)[None, :]
+    Wg = (i - c).astype(np.float32)
+    Wu = (i + 2 * c + 1).astype(np.float32)
+    x = np.array([1.0, -1.0, 2.0, 0.5], dtype=np.float32)
+    g = Wg.astype(np.float64) @ x.astype(np.float64)
+    u = Wu.astype(np.float64) @ x.astype(np.float64)
+    assert len(set(g.tolist()) | set(u.tolist())) == 2 * nf
+    return np.concatenate([Wg, Wu]), x, g, u
+
+
+def pin_ffn_gate_up_pairing(orc):
+    """out[i] = SiLU(gate_i) * up_i with gate from row i and up from row nf + i of the concat
+    weight: checked against mpmath at correctly rounded f32, for f32 and bf16 weights."""
+    import mpmath
+    mpmath.mp.dps = 50
+    W, x, g, u = _ffn_hand_case()
+    want = np.array([_mp_round_f32(mpmath.mpf(gi) / (1 + mpmath.exp(-mpmath.mpf(gi))) * mpmath.mpf(ui))
+                     for gi, ui in zip(g, u)], dtype=np.float32)
+    for enc in (W, bf16_bits_exact(W)):
+        got = orc.ffn_swiglu(enc, x)
+        assert got.shape == (3,)
+        # the double-precision result may sit one f32 ulp from the exact one only at a tie
+        assert np.all(np.abs(f32_bits(got).astype(np.int64) - f32_bits(want).astype(np.int64)) <= 1), (got, want)
+
+
+def pin_ffn_zero_gate_and_unit_up(orc):
+    """A zero gate row gives 0 whatever the up row; a gate row of e_0 with x_0 = ln 3 and an
+    up row of 4 e_0 gives SiLU(ln 3) * 4 ln 3 = 3 (ln 3)^2."""
+    ln3 = np.float32(math.log(3.0))
+    x = np.array([ln3, 5.0], dtype=np.float32)
+    W = np.array([[0.0, 0.0],    # gate 0: zero
+                  [1.0, 0.0],    # gate 1: x0
+                  [7.0, -3.0],   # up 0: anything
+                  [4.0, 0.0]],   # up 1: 4 x0
+                 dtype=np.float32)
+    out = orc.ffn_swiglu(W, x)
+    assert out[0] == 0.0
+    want = 3.0 * float(ln3) ** 2
+    assert abs(float(out[1]) - want) <= 2e-7 * want
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

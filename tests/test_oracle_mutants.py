@@ -42,6 +42,15 @@ MUTANTS = {
                         "return (float)((double)pos * (double)inv_freq * (1.0 + 1e-7));"),
     "stage_skips_k_rope": ("oracle_rope_pair(yk[j], yk[j2], bk[j], bk[j2], pos, f,",
                            "oracle_rope_pair(yk[j], yk[j2], bk[j], bk[j2], 0, f,"),
+    "silu_sign": ("return v / (1.0 + exp(-v));", "return v / (1.0 + exp(v));"),
+    "silu_is_sigmoid": ("return v / (1.0 + exp(-v));", "return 1.0 / (1.0 + exp(-v));"),
+    "ffn_gate_up_swapped": ("out[i] = (float)(oracle_silu(g) * u);", "out[i] = (float)(oracle_silu(u) * g);"),
+    "ffn_up_row_reversed": ("const float* ru = (const float*)W + (nf + i) * H;",
+                            "const float* ru = (const float*)W + (2 * nf - 1 - i) * H;"),
+    "ffn_up_row_reversed_bf16": ("const uint16_t* ru = (const uint16_t*)W + (nf + i) * H;",
+                                 "const uint16_t* ru = (const uint16_t*)W + (2 * nf - 1 - i) * H;"),
+    "ffn_drops_last_column": ("for (int64_t c = 0; c < H; ++c) {\n                g += (double)rg[c]",
+                              "for (int64_t c = 0; c + 1 < H; ++c) {\n                g += (double)rg[c]"),
 }
 
 
