@@ -47,7 +47,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", default=configs.QWEN14B.name, choices=sorted(configs.WORKLOADS))
+    ap.add_argument("--workload", default=configs.QWEN14B.name,
+                    choices=sorted(configs.WORKLOADS) + sorted(configs.FFN_WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="bound on the oracle's CPU-baseline sample")
     ap.add_argument("--no-e2e", action="store_true")
@@ -460,8 +461,166 @@ def prefill_arm(args, w):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------- FusedFFN workloads
+
+FFN_METRIC = "decode FusedFFN (gate|up GEMV + SwiGLU) layers/sec and achieved HBM GB/s, 1 GPU"
+
+
+def ffn_config(w):
+    return {"workload": w.name, "layers": w.n_layers, "hidden": w.hidden, "n_ff": w.n_ff,
+            "w_dtype": w.w_dtype,
+            "l2": ("inputs larger than L2: %.2f GB of weights per step" % (w.n_layers * w.w_bytes() / 1e9))
+            if w.n_layers * w.w_bytes() > 4 * L2_BYTES else "weights fit in L2 (hot)",
+            "parallelism": "replicas"}
+
+
+def ffn_arm(args, w):
+    import torch
+    import qkv_rope_kv_gb300 as Q
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    Q.load()
+    seed = rank
+    L = w.n_layers
+    dt = Q.QKV_BF16 if w.w_dtype == "bf16" else Q.QKV_F32
+    dx = torch.empty(L, w.hidden, dtype=torch.float32, device="cuda")
+    dout = torch.zeros(L, w.n_ff, dtype=torch.float32, device="cuda")
+    hostW = np.empty((2 * w.n_ff, w.hidden), np.uint16 if w.w_dtype == "bf16" else np.float32)
+    layers, keep = [], []
+    for l in range(L):
+        synth.ffn_weight_rows(seed, l, 0, 2 * w.n_ff, w.hidden, w.w_dtype, out=hostW)
+        dW = torch.from_numpy(hostW.view(np.int16) if w.w_dtype == "bf16" else hostW).to("cuda")
+        keep.append(dW)
+        layers.append(dict(x=dx[l], w_gate_up=dW, out=dout[l]))
+    h_in = torch.from_numpy(np.stack([synth.hidden(seed, 100 + l, 0, w.hidden) for l in range(L)])).pin_memory()
+    dx.copy_(h_in)
+    h_out = torch.empty(L, w.n_ff, dtype=torch.float32).pin_memory()
+    stream = torch.cuda.Stream()
+    graph = Q.qkv_ffn_graph_create(w.hidden, w.n_ff, dt, layers, stream)
+    for _ in range(max(args.warmup, 3)):
+        graph.launch(stream)
+    stream.synchronize()
+    flags, _ = Q.qkv_check_device_error(stream)
+    if flags:
+        raise RuntimeError("device status flags set during warm-up: %#x" % flags)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    barrier_sync(world)
+    elapsed = time_replays(lambda: graph.launch(stream), args.steps, stream)
+    barrier_sync(world)
+    clk = clocks.stop()
+    elapsed = max_over_ranks(elapsed, world)
+    e2e = None
+    if not args.no_e2e:
+        for _ in range(3):
+            graph.run_host(h_in, dx, dout, h_out, stream)
+        barrier_sync(world)
+        e_el = time_replays(lambda: graph.run_host(h_in, dx, dout, h_out, stream), args.steps, stream)
+        barrier_sync(world)
+        e_el = max_over_ranks(e_el, world)
+        e2e = {"value": world * L * args.steps / e_el, "unit": "layers/s",
+               "h2d_bytes_per_step": int(h_in.numel() * 4), "d2h_bytes_per_step": int(h_out.numel() * 4),
+               "ms_per_step": 1e3 * e_el / args.steps,
+               "path": "qkv_model_graph_run_host: pinned host x block -> device, graph replay, "
+                       "SwiGLU outputs of all layers -> pinned host"}
+    per_layer = elapsed / args.steps / L
+    algo = w.algo_bytes_per_layer()
+    peak, peak_kind = measured_peak()
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        v, n, s = ffn_oracle_layers_per_s(w, seed, args.cpu_seconds, max_layers=L)
+        cpu = {"value": v, "unit": "layers/s", "cores": 1, "kind": "oracle",
+               "sample": "%d consecutive layers of %s (%.1f s of oracle time), single-threaded C oracle, "
+                         "weight generation excluded" % (n, w.name, s)}
+    if rank == 0:
+        line = {
+            "metric": FFN_METRIC, "value": world * L * args.steps / elapsed, "unit": "layers/s",
+            "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+            "ms_per_step": 1e3 * elapsed / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded SplitMix64/Box-Muller weights ~N(0,0.02), x ~N(0,1); "
+                    "bf16 weights widened exactly, f32 accumulate)",
+            "config": ffn_config(w),
+            "hbm_gbs": algo / per_layer / 1e9,
+            "roofline": {"bound": "hbm", "achieved": algo / per_layer / 1e9, "peak": peak, "unit": "GB/s",
+                         "frac": algo / per_layer / 1e9 / peak, "peak_kind": peak_kind,
+                         "frac_of_nominal_8000": algo / per_layer / 1e9 / NOMINAL_HBM_GBS,
+                         "traffic": None, "algo_bytes_per_launch": algo,
+                         "kernel": "qkv_decode_blk_kernel (gate|up GEMV + SwiGLU tail)",
+                         "duration_basis": "step time / %d launches (back-to-back graph replay)" % L},
+            "e2e": e2e, "cpu_baseline": cpu,
+            "gpu_launches": graph.kernel_count * args.steps, "launches_per_step": graph.kernel_count,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def ffn_oracle_layers_per_s(w, seed: int, seconds: float, max_layers: int | None = None):
+    """Time the FusedFFN oracle (single thread, as it stands) over consecutive layers."""
+    import oracle
+    orc = oracle.Oracle()
+    done, spent, l = 0, 0.0, 0
+    while (done == 0 or spent < seconds) and (max_layers is None or done < max_layers):
+        layer = l % w.n_layers
+        W = synth.ffn_weight_rows(seed, layer, 0, 2 * w.n_ff, w.hidden, w.w_dtype)
+        x = synth.hidden(seed, 100 + layer, 0, w.hidden)
+        t0 = time.perf_counter()
+        orc.ffn_swiglu(W, x)
+        spent += time.perf_counter() - t0
+        done += 1
+        l += 1
+    return done / spent, done, spent
+
+
+def ffn_reference_arm(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    seed = 0
+    for _ in range(args.warmup):
+        ffn_oracle_layers_per_s(w, seed, 0.0, max_layers=1)
+    total_layers, total_s = 0, 0.0
+    for _ in range(args.steps):
+        _, n, s = ffn_oracle_layers_per_s(w, seed, 0.0, max_layers=1)
+        total_layers += n
+        total_s += s
+    value = total_layers / total_s
+    line = {
+        "impl": "reference", "metric": FFN_METRIC, "value": value, "unit": "layers/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded SplitMix64/Box-Muller weights and x)",
+        "config": ffn_config(w),
+        "cpu_baseline": {"value": value, "unit": "layers/s", "cores": 1, "kind": "oracle",
+                         "sample": "%d steps x 1 layer of %s, single-threaded C oracle (double "
+                                   "accumulation), weight generation excluded" % (args.steps, w.name)},
+        "e2e": {"value": value, "unit": "layers/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
+    if args.workload in configs.FFN_WORKLOADS:
+        import dataclasses
+        w = configs.FFN_WORKLOADS[args.workload]
+        if args.layers is not None:
+            w = dataclasses.replace(w, name=w.name + "-first%d-layers-profiling-only" % args.layers,
+                                    n_layers=args.layers)
+        if args.impl == "reference":
+            ffn_reference_arm(args, w)
+        else:
+            ffn_arm(args, w)
+        return
     w = configs.WORKLOADS[args.workload]
     if args.layers is not None:
         import dataclasses

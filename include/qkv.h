@@ -274,6 +274,45 @@ qkv_status qkv_prefill_graph_create(const qkv_plan* const* plans, int32_t n_laye
                                     const qkv_prefill_ptrs* layers, int32_t nt, void* stream,
                                     qkv_graph** out);
 
+/* ---- FusedFFN decode: the FFN's gate|up projection and SwiGLU --------------- */
+
+/* One token of the FFN activation of page "06 · Assign + fusion — every node
+ * picks an engine, then patterns fold", §2.2 (gate = W_gate x, up = W_up x of
+ * the normed hidden state; SiLU(v) = v * sigmoid(v); their elementwise
+ * product) in the decode form of §2.3 (one concat gate|up weight, then the
+ * offset SwiGLU over the two halves of its output), as one launch:
+ *   out[i] = silu(g_i) * u_i,  g_i = sum_c W[i][c] x[c],  u_i = sum_c W[nf + i][c] x[c].
+ * The down projection that follows is not part of it.
+ *   hidden      H (1 .. 49152).
+ *   n_ff        nf, the intermediate size (>= 1).
+ *   w_dtype     QKV_F32 or QKV_BF16.
+ *   x           device, H floats, 16-byte aligned.
+ *   w_gate_up   device, [2 nf x H] row-major: rows 0 .. nf-1 are W_gate,
+ *               rows nf .. 2nf-1 W_up; 16-byte aligned.
+ *   out         device, nf floats.
+ * f32 accumulation over bf16 weights widened exactly; g and u are rounded to
+ * f32, then silu(g) = g / (1 + e^-g) and the product are f32 operations.
+ * Caller-owned memory only; nothing is allocated.
+ * Errors: INVALID_ARG (null or misaligned pointers, sizes out of range),
+ * UNSUPPORTED (H * element size not a multiple of 16 bytes), CUDA. */
+qkv_status qkv_ffn_step(int32_t hidden, int32_t n_ff, int32_t w_dtype, const float* x,
+                        const void* w_gate_up, float* out, void* stream);
+
+/* Per-layer buffers of an FFN graph layer, as in qkv_ffn_step. */
+typedef struct qkv_ffn_layer {
+    const float* x;
+    const void* w_gate_up;
+    float* out;
+} qkv_ffn_layer;
+
+/* Capture n_layers FusedFFN steps of one shape into a CUDA graph, chained with
+ * programmatic dependent launch as in qkv_model_graph_create (a layer streams
+ * its weights while the previous one finishes, and reads x and writes out only
+ * after it completed); replay it with qkv_model_graph_launch.  Errors as
+ * qkv_model_graph_create and qkv_ffn_step. */
+qkv_status qkv_ffn_graph_create(int32_t hidden, int32_t n_ff, int32_t w_dtype, int32_t n_layers,
+                                const qkv_ffn_layer* layers, void* stream, qkv_graph** out);
+
 /* Number of kernel nodes in the graph (launches per decode step). */
 qkv_status qkv_model_graph_kernel_count(const qkv_graph* graph, int32_t* out);
 void qkv_model_graph_destroy(qkv_graph* graph);

@@ -73,6 +73,10 @@ class qkv_prefill_ptrs(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("X", "w", "bias", "positions", "Y", "kv_k", "kv_v")]
 
 
+class qkv_ffn_layer(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("x", "w_gate_up", "out")]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -118,6 +122,8 @@ def _declare(lib):
         "qkv_model_graph_create": ([vp, i32, vp, vp, vp, ctypes.POINTER(vp)], st),
         "qkv_model_graph_launch": ([vp, vp], st),
         "qkv_prefill_graph_create": ([vp, i32, vp, i32, vp, ctypes.POINTER(vp)], st),
+        "qkv_ffn_step": ([i32, i32, i32, vp, vp, vp, vp], st),
+        "qkv_ffn_graph_create": ([i32, i32, i32, i32, vp, vp, ctypes.POINTER(vp)], st),
         "qkv_model_graph_run_host": ([vp, vp, vp, sz, vp, vp, sz, vp], st),
         "qkv_model_graph_kernel_count": ([vp, ctypes.POINTER(i32)], st),
         "qkv_model_graph_destroy": ([vp], None),
@@ -311,6 +317,25 @@ def qkv_prefill_graph_create(plans, layers, nt: int, stream) -> ModelGraph:
     h = ctypes.c_void_p()
     _check(_lib.qkv_prefill_graph_create(arr_plans, n, arr_layers, nt, _stream(stream), ctypes.byref(h)))
     return ModelGraph(h.value, (plans, layers))
+
+
+# ---------------------------------------------------------------- FusedFFN
+
+def qkv_ffn_step(hidden: int, n_ff: int, w_dtype: int, x, w_gate_up, out, stream=None):
+    """out[i] = silu(g_i) * u_i over the concat gate|up weight (device tensors)."""
+    _check(_lib.qkv_ffn_step(hidden, n_ff, w_dtype, _ptr(x), _ptr(w_gate_up), _ptr(out), _stream(stream)))
+
+
+def qkv_ffn_graph_create(hidden: int, n_ff: int, w_dtype: int, layers, stream) -> ModelGraph:
+    """``layers``: list of dicts with the qkv_ffn_layer field names -> tensors."""
+    n = len(layers)
+    arr = (qkv_ffn_layer * n)()
+    for i, L in enumerate(layers):
+        for name, _ in qkv_ffn_layer._fields_:
+            setattr(arr[i], name, _ptr(L.get(name)))
+    h = ctypes.c_void_p()
+    _check(_lib.qkv_ffn_graph_create(hidden, n_ff, w_dtype, n, arr, _stream(stream), ctypes.byref(h)))
+    return ModelGraph(h.value, (layers,))
 
 
 # ---------------------------------------------------------------- device status

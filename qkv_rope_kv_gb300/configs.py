@@ -62,3 +62,29 @@ QWEN14B_PREFILL = Workload("qwen2.5-14b-prefill-nt128", 5120, 40, 8, 128, "bf16"
                            tuple(range(128)), nt=128)
 
 WORKLOADS = {w.name: w for w in (QWEN05_SINGLE, QWEN05_SWEEP, QWEN7B, QWEN14B, QWEN14B_PREFILL)}
+
+
+@dataclass(frozen=True)
+class FfnWorkload:
+    """Decode FusedFFN (gate|up projection + SwiGLU) over n_layers layers of one shape."""
+    name: str
+    hidden: int
+    n_ff: int
+    w_dtype: str            # "f32" or "bf16"
+    n_layers: int
+
+    def w_bytes(self) -> int:
+        return 2 * self.n_ff * self.hidden * (4 if self.w_dtype == "f32" else 2)
+
+    def algo_bytes_per_layer(self) -> int:
+        """Bytes one layer must move: the gate|up weight and x read, nf outputs written."""
+        return self.w_bytes() + 4 * self.hidden + 4 * self.n_ff
+
+
+# Intermediate sizes: 4864 for 0.5B is printed on page 06 (§2.2); 13824 (14B) and
+# 18944 (7B) are the public Qwen2.5 model configurations.
+QWEN05_FFN = FfnWorkload("qwen2.5-0.5b-ffn-24layer", 896, 4864, "f32", 24)
+QWEN7B_FFN = FfnWorkload("qwen2.5-7b-ffn-28layer", 3584, 18944, "bf16", 28)
+QWEN14B_FFN = FfnWorkload("qwen2.5-14b-ffn-48layer", 5120, 13824, "bf16", 48)
+
+FFN_WORKLOADS = {w.name: w for w in (QWEN05_FFN, QWEN7B_FFN, QWEN14B_FFN)}

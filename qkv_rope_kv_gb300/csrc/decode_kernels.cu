@@ -607,6 +607,37 @@ __global__ void __launch_bounds__((kGroups * kGroupWarps + 1) * 32, 2)
 #endif
 constexpr int kBlkPairs = QKV_DECODE_BLOCK_PAIRS;  // rows per stage (one contiguous bulk copy)
 
+// What the block ring computes after the projection.
+enum BlockEpilogue {
+    kEpiQkv = 0,     // bias, neox RoPE on q/k, KV-cache store (units: neox pairs of a head, v rows)
+    kEpiSwiglu = 1,  // silu(gate) * up (units: rows i of the gate half with rows nf + i)
+};
+
+template <int EPI>
+__device__ __forceinline__ int blk_unit_count(const DecodeParams& p) {
+    if constexpr (EPI == kEpiQkv) return unit_count<kBlkPairs>(p.nqt, p.nkt, p.hd);
+    else return (p.nf + kBlkPairs - 1) / kBlkPairs;
+}
+
+template <int EPI>
+__device__ __forceinline__ Unit blk_unit(int u, const DecodeParams& p) {
+    if constexpr (EPI == kEpiQkv) {
+        return unit_info<kBlkPairs>(u, p.nqt, p.nkt, p.hd);
+    } else {
+        Unit t;
+        t.sec = 0;
+        t.r = u * kBlkPairs;
+        t.n = min(kBlkPairs, p.nf - t.r);
+        t.off = p.nf;
+        return t;
+    }
+}
+
+// SwiGLU of one (gate, up) pair, each step rounded to f32: silu(g) = g / (1 + e^-g).
+__device__ __forceinline__ float swiglu(float g, float u) {
+    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+}
+
 // Block ring: a unit of kBlkPairs neox pairs has two row blocks, (h*hd + d0 ..)
 // and (h*hd + hd/2 + d0 ..); each block is one stage, filled by one contiguous
 // bulk copy.  Item i of a CTA is block (i & 1) of its unit i >> 1 (a contiguous
@@ -615,8 +646,10 @@ constexpr int kBlkPairs = QKV_DECODE_BLOCK_PAIRS;  // rows per stage (one contig
 // memory and bumps the unit's counter; the second of the two blocks to finish
 // rotates the unit's pairs and stores them, one pair per lane.  v blocks need
 // no partner and finish on their own.  Each row is reduced exactly as in the
-// pair ring (dot2_staged), so both kernels give the same bits.
-template <typename WT, int MODE, int kGroups>
+// pair ring (dot2_staged), so both kernels give the same bits.  With
+// EPI = kEpiSwiglu the same ring runs the FusedFFN: a unit pairs gate rows
+// (i ..) with up rows (nf + i ..), and the second block writes silu(g) * u.
+template <typename WT, int MODE, int kGroups, int EPI>
 __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
     qkv_decode_blk_kernel(const __grid_constant__ DecodeParams p, int stages, uint32_t stage_bytes,
                           uint32_t x_bytes, int max_units) {
@@ -633,7 +666,7 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
     int* cnt = reinterpret_cast<int*>(res + max_units * 2 * kBlkPairs);  // [max_units]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int units = unit_count<kBlkPairs>(p.nqt, p.nkt, p.hd);
+    const int units = blk_unit_count<EPI>(p);
     const int u_begin = static_cast<int>(static_cast<long long>(units) * blockIdx.x / gridDim.x);
     const int u_end = static_cast<int>(static_cast<long long>(units) * (blockIdx.x + 1) / gridDim.x);
     const int n = 2 * (u_end - u_begin);
@@ -663,7 +696,7 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
                     flag_timeout();
                     break;
                 }
-                const Unit t = unit_info<kBlkPairs>(u_begin + (i >> 1), p.nqt, p.nkt, p.hd);
+                const Unit t = blk_unit<EPI>(u_begin + (i >> 1), p);
                 const int rb = (i & 1) ? t.r + t.off : t.r;
                 const uint32_t bytes = static_cast<uint32_t>(t.n) * row_bytes;
                 const unsigned char* w = static_cast<const unsigned char*>(p.w[t.sec]);
@@ -683,11 +716,11 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
     // ---- consumers ----
     // Biases are parameters, not outputs of an earlier kernel: stage this CTA's
     // share before the dependency wait, so no global load sits in the item loop.
-    if (MODE == kFused) {
+    if (MODE == kFused && EPI == kEpiQkv) {
         const int nb = (u_end - u_begin) * 2 * kBlkPairs;
         for (int e = threadIdx.x; e < nb; e += kGroups * 32) {
             const int j = e % kBlkPairs, blk = (e / kBlkPairs) & 1, ul = e / (2 * kBlkPairs);
-            const Unit t = unit_info<kBlkPairs>(u_begin + ul, p.nqt, p.nkt, p.hd);
+            const Unit t = blk_unit<EPI>(u_begin + ul, p);
             bias_s[e] = j < t.n ? __ldg(p.bias[t.sec] + (blk ? t.r + t.off : t.r) + j) : 0.f;
         }
     }
@@ -705,12 +738,13 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
         } else {
             for (int c = tid; c < nch; c += nthr) xs4[c] = xg[c];
         }
-        for (int i = tid; i < (p.hd >> 1); i += nthr) freq_s[i] = p.inv_freq[i];
+        if (EPI == kEpiQkv)
+            for (int i = tid; i < (p.hd >> 1); i += nthr) freq_s[i] = p.inv_freq[i];
     }
     named_barrier_sync(1, kGroups * 32);
-    const int pos = (MODE == kFused) ? *p.pos : 0;
+    const int pos = (MODE == kFused && EPI == kEpiQkv) ? *p.pos : 0;
     const bool store = pos_ok(pos, p.n_ctx);
-    if (MODE == kFused && !store && blockIdx.x == 0 && threadIdx.x == 0) flag_bad_pos(pos);
+    if (MODE == kFused && EPI == kEpiQkv && !store && blockIdx.x == 0 && threadIdx.x == 0) flag_bad_pos(pos);
 
     for (int i = warp; i < n; i += kGroups) {
         const int st = i % stages;
@@ -719,7 +753,7 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
             break;
         }
         const int ul = i >> 1, blk = i & 1;
-        const Unit t = unit_info<kBlkPairs>(u_begin + ul, p.nqt, p.nkt, p.hd);
+        const Unit t = blk_unit<EPI>(u_begin + ul, p);
         const int rb = blk ? t.r + t.off : t.r;
         const unsigned char* sp = ring + static_cast<size_t>(st) * stage_bytes;
         float y[kBlkPairs];
@@ -740,7 +774,23 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
         for (int j = 1; j < kBlkPairs; ++j)
             if (lane == j) yl = y[j];
         const int e = (ul * 2 + blk) * kBlkPairs + lane;
-        if constexpr (MODE == kProjectOnly) {
+        if constexpr (EPI == kEpiSwiglu) {
+            if (lane < t.n) res[e] = yl;
+            __syncwarp();
+            int first = 0;
+            if (lane == 0) {
+                __threadfence_block();
+                first = atomicAdd(&cnt[ul], 1);
+                __threadfence_block();
+            }
+            first = __shfl_sync(0xffffffffu, first, 0);
+            __syncwarp();
+            if (first == 1 && lane < t.n) {
+                // the partner block is complete: gate from block 0, up from block 1
+                const float o = static_cast<volatile float*>(res)[e + (blk ? -kBlkPairs : kBlkPairs)];
+                p.out[0][t.r + lane] = swiglu(blk ? o : yl, blk ? yl : o);
+            }
+        } else if constexpr (MODE == kProjectOnly) {
             if (lane < t.n) p.out[t.sec][rb + lane] = yl;
         } else if (t.sec == 2) {
             if (lane < t.n) epi_v_elem_b(p, rb + lane, yl, bias_s[e], pos, store);
@@ -912,14 +962,14 @@ cudaError_t launch_decode_tma(const DecodeParams& p, const RingShape& r, bool pd
 
 
 // Block ring in a dynamic shared-memory budget (0 stages: does not fit).
-template <typename WT, int MODE, int kGroups>
+template <typename WT, int MODE, int kGroups, int EPI = kEpiQkv>
 cudaError_t launch_decode_blk(const DecodeParams& p, int ctas_per_sm, int smem_kb, bool pdl, cudaStream_t stream,
                               bool& launched) {
     launched = false;
     const size_t row = static_cast<size_t>(p.H) * sizeof(WT);
     const uint32_t stage_bytes = static_cast<uint32_t>((kBlkPairs * row + 127) / 128 * 128);
     const uint32_t x_bytes = static_cast<uint32_t>((static_cast<size_t>(p.H) * 4 + 127) / 128 * 128);
-    const int units = unit_count<kBlkPairs>(p.nqt, p.nkt, p.hd);
+    const int units = EPI == kEpiQkv ? unit_count<kBlkPairs>(p.nqt, p.nkt, p.hd) : (p.nf + kBlkPairs - 1) / kBlkPairs;
     const int ctas_max = sm_count() * ctas_per_sm;
     const int grid = units < ctas_max ? units : ctas_max;
     const int max_units = (units + grid - 1) / grid;
@@ -931,7 +981,7 @@ cudaError_t launch_decode_blk(const DecodeParams& p, int ctas_per_sm, int smem_k
     int stages = static_cast<int>((budget - fixed) / stage_bytes);
     stages = stages > kMaxStages ? kMaxStages : stages;
     stages -= stages % kGroups;
-    auto kernel = qkv_decode_blk_kernel<WT, MODE, kGroups>;
+    auto kernel = qkv_decode_blk_kernel<WT, MODE, kGroups, EPI>;
     const size_t smem = x_bytes + static_cast<size_t>(stages) * stage_bytes + 2 * stages * sizeof(uint64_t) + tail;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
@@ -982,7 +1032,25 @@ cudaError_t launch_decode_t(const DecodeParams& p, bool pdl, cudaStream_t stream
     return launch_ex(kernel, dim3(grid), dim3(wpc * 32), smem, pdl, stream, p);
 }
 
+template <typename WT>
+cudaError_t launch_ffn_t(const DecodeParams& p, bool pdl, cudaStream_t stream) {
+    const size_t row = static_cast<size_t>(p.H) * sizeof(WT);
+    bool launched = false;
+    const cudaError_t e =
+        row >= kSmallRowBytes
+            ? launch_decode_blk<WT, kFused, kGroupsLarge, kEpiSwiglu>(p, QKV_DECODE_LARGE_CTAS, QKV_DECODE_LARGE_SMEM_KB,
+                                                                     pdl, stream, launched)
+            : launch_decode_blk<WT, kFused, kGroupsSmall, kEpiSwiglu>(p, QKV_DECODE_SMALL_CTAS, QKV_DECODE_SMALL_SMEM_KB,
+                                                                     pdl, stream, launched);
+    if (e != cudaSuccess) return e;
+    return launched ? cudaSuccess : cudaErrorNotSupported;
+}
+
 }  // namespace
+
+cudaError_t launch_ffn(const DecodeParams& p, int w_dtype, bool pdl, cudaStream_t stream) {
+    return w_dtype == QKV_BF16 ? launch_ffn_t<uint16_t>(p, pdl, stream) : launch_ffn_t<float>(p, pdl, stream);
+}
 
 cudaError_t launch_decode(const DecodeParams& p, int w_dtype, int vec, DecodeMode mode, bool pdl,
                           cudaStream_t stream) {

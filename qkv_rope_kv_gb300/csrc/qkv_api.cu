@@ -364,6 +364,45 @@ extern "C" qkv_status qkv_prefill_step(const qkv_plan* plan, const uint16_t* X, 
     return run_prefill(plan, X, nt, w, bias, d_positions, Y, kv_k, kv_v, false, static_cast<cudaStream_t>(stream));
 }
 
+// ------------------------------------------------------------------ FusedFFN
+
+namespace {
+
+qkv_status check_ffn(int32_t H, int32_t nf, int32_t w_dtype, const float* x, const void* w, const float* out) {
+    REQUIRE(H >= 1 && H <= 49152, "hidden %d out of range 1 .. 49152", H);
+    REQUIRE(nf >= 1, "n_ff must be >= 1");
+    REQUIRE(w_dtype == QKV_F32 || w_dtype == QKV_BF16, "w_dtype must be QKV_F32 or QKV_BF16");
+    REQUIRE(x && w && out, "null x, w_gate_up or out");
+    REQUIRE(aligned16(x) && aligned16(w), "x and w_gate_up must be 16-byte aligned");
+    if ((static_cast<int64_t>(H) * elem_size(w_dtype)) % 16 != 0)
+        return fail(QKV_ERR_UNSUPPORTED, "hidden * element size must be a multiple of 16 bytes");
+    return QKV_OK;
+}
+
+qkv_status run_ffn(int32_t H, int32_t nf, int32_t w_dtype, const float* x, const void* w, float* out, bool pdl,
+                   cudaStream_t s) {
+    DecodeParams p;
+    std::memset(&p, 0, sizeof p);
+    p.x = x;
+    p.w[0] = w;
+    p.out[0] = out;
+    p.H = H;
+    p.nf = nf;
+    const cudaError_t e = launch_ffn(p, w_dtype, pdl, s);
+    if (e == cudaErrorNotSupported) return fail(QKV_ERR_UNSUPPORTED, "hidden %d leaves no room for the ring", H);
+    if (e != cudaSuccess) return cuda_fail(e, "FusedFFN kernel launch");
+    return QKV_OK;
+}
+
+}  // namespace
+
+extern "C" qkv_status qkv_ffn_step(int32_t hidden, int32_t n_ff, int32_t w_dtype, const float* x,
+                                   const void* w_gate_up, float* out, void* stream) {
+    qkv_status st = check_ffn(hidden, n_ff, w_dtype, x, w_gate_up, out);
+    if (st != QKV_OK) return st;
+    return run_ffn(hidden, n_ff, w_dtype, x, w_gate_up, out, false, static_cast<cudaStream_t>(stream));
+}
+
 // ------------------------------------------------------------------ cache view
 
 extern "C" qkv_status kv_cache_view(const qkv_plan* plan, void* kv_k, void* kv_v, qkv_kv_view* out) {
@@ -493,6 +532,26 @@ qkv_status finish_capture(cudaStream_t s, qkv_status st, qkv_graph** out) {
 }
 
 }  // namespace
+
+extern "C" qkv_status qkv_ffn_graph_create(int32_t hidden, int32_t n_ff, int32_t w_dtype, int32_t n_layers,
+                                           const qkv_ffn_layer* layers, void* stream, qkv_graph** out) {
+    REQUIRE(out, "out is null");
+    *out = nullptr;
+    REQUIRE(layers, "layers is null");
+    REQUIRE(n_layers >= 1, "n_layers must be >= 1");
+    REQUIRE(stream, "capture needs a non-default stream");
+    for (int32_t i = 0; i < n_layers; ++i) {
+        qkv_status st = check_ffn(hidden, n_ff, w_dtype, layers[i].x, layers[i].w_gate_up, layers[i].out);
+        if (st != QKV_OK) return fail(st, "layer %d: %s", i, g_last_error.c_str());
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamBeginCapture");
+    qkv_status st = QKV_OK;
+    for (int32_t i = 0; i < n_layers && st == QKV_OK; ++i)
+        st = run_ffn(hidden, n_ff, w_dtype, layers[i].x, layers[i].w_gate_up, layers[i].out, i > 0, s);
+    return finish_capture(s, st, out);
+}
 
 extern "C" qkv_status qkv_prefill_graph_create(const qkv_plan* const* plans, int32_t n_layers,
                                                const qkv_prefill_ptrs* layers, int32_t nt, void* stream,

@@ -25,6 +25,7 @@ struct DecodeParams {
     void* kv_v;             // V region [n_ctx x nkt]
     const int32_t* pos;     // device position
     int32_t H, nqt, nkt, hd, n_ctx, kv_f16;
+    int32_t nf;             // FusedFFN: rows per half of the gate|up weight (0 for the QKV stage)
     float inv_freq[QKV_MAX_HEAD_DIM / 2];
 };
 
@@ -39,6 +40,10 @@ cudaError_t launch_chain_rope(const DecodeParams& p, float* y, int n_heads, cuda
 cudaError_t launch_chain_store(const DecodeParams& p, const float* src, void* cache,
                                cudaStream_t stream);
 cudaError_t device_status_read(cudaStream_t stream, uint32_t* flags, int32_t* bad_pos);
+// FusedFFN decode: out[i] = silu((W x)[i]) * (W x)[nf + i] over the concat gate|up
+// weight p.w[0] [2 nf x H] into p.out[0] [nf]; rows must be 16-byte aligned.
+// Returns cudaErrorNotSupported when no ring shape fits the hidden size.
+cudaError_t launch_ffn(const DecodeParams& p, int w_dtype, bool pdl, cudaStream_t stream);
 
 // prefill_tcgen05.cu
 struct PrefillParams {

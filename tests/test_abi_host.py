@@ -153,3 +153,24 @@ def test_graph_create_guards(lib):
     assert lib.qkv_model_graph_create(plans, 1, layers, 16, None, ctypes.byref(h)) == q.QKV_ERR_INVALID_ARG
     # layer 0 has null pointers: rejected before any capture starts
     assert lib.qkv_model_graph_create(plans, 1, layers, 16, 16, ctypes.byref(h)) == q.QKV_ERR_INVALID_ARG
+
+
+def test_ffn_guards(lib):
+    """FusedFFN arguments are validated on the host before any CUDA call."""
+    f = lib.qkv_ffn_step
+    ok = 16 * 64  # a 16-byte aligned stand-in address; nothing is dereferenced on failure
+    assert f(0, 8, q.QKV_BF16, ok, ok, ok, None) == q.QKV_ERR_INVALID_ARG          # hidden < 1
+    assert f(49160, 8, q.QKV_BF16, ok, ok, ok, None) == q.QKV_ERR_INVALID_ARG      # hidden > 49152
+    assert f(64, 0, q.QKV_BF16, ok, ok, ok, None) == q.QKV_ERR_INVALID_ARG         # n_ff < 1
+    assert f(64, 8, q.QKV_F16, ok, ok, ok, None) == q.QKV_ERR_INVALID_ARG          # f16 weights
+    assert f(64, 8, q.QKV_BF16, None, ok, ok, None) == q.QKV_ERR_INVALID_ARG       # null x
+    assert f(64, 8, q.QKV_BF16, ok + 4, ok, ok, None) == q.QKV_ERR_INVALID_ARG     # misaligned x
+    assert f(64, 8, q.QKV_BF16, ok, ok + 8, ok, None) == q.QKV_ERR_INVALID_ARG     # misaligned weights
+    assert f(12, 8, q.QKV_BF16, ok, ok, ok, None) == q.QKV_ERR_UNSUPPORTED         # 24-byte rows
+    h = ctypes.c_void_p()
+    layers = (q.qkv_ffn_layer * 1)()
+    g = lib.qkv_ffn_graph_create
+    assert g(64, 8, q.QKV_BF16, 0, layers, 16, ctypes.byref(h)) == q.QKV_ERR_INVALID_ARG
+    assert g(64, 8, q.QKV_BF16, 1, layers, None, ctypes.byref(h)) == q.QKV_ERR_INVALID_ARG
+    assert g(64, 8, q.QKV_BF16, 1, layers, 16, ctypes.byref(h)) == q.QKV_ERR_INVALID_ARG  # null layer 0
+
