@@ -8,26 +8,26 @@
 // the per-token math is the decode math of §3.2 Excerpt A at pos = positions[t],
 // computed by the same device functions (epilogue_math.cuh).
 //
-// Tiling.  One CTA computes a tile of 128 tokens (UMMA M) x 64 weight rows
-// (UMMA N).  The 64 rows are two 32-row boxes chosen so that every neox pair
-// lands in one thread: for a q or k tile, rows (h*hd + d0 .. +31) and
-// (h*hd + hd/2 + d0 .. +31); for a v tile, 64 consecutive rows.  K advances in
-// blocks of 64 bf16 (128 bytes, one 128B-swizzle row).  CTAs of a thread-block
-// cluster (CN consecutive row tiles, same tokens) share X: each loads a 1/CN
-// slice of every X stage with TMA multicast, so one L2 read feeds CN CTAs.
-// Warp 0 lane 0 streams W boxes into a 6-stage ring (before the dependency wait:
-// weights are parameters) and warp 2 lane 0 its X slices into a 4-stage ring
-// (mbarrier transaction counts; an X stage is reused once all CN CTAs of the
-// cluster released it);
-// warp 1 lane 0 issues tcgen05.mma (kind::f16, bf16 x bf16 -> f32 in TMEM,
-// 4 MMAs of K = 16 per block) and releases each stage in every CTA of the cluster
-// with a multicast tcgen05.commit; then
-// all four warps read their 32 TMEM lanes (one token each) with tcgen05.ld and
-// run the epilogue: Y leaves through shared memory (128-byte swizzle) and two
-// TMA tensor stores, the token's k/v cache rows as 16-byte stores.  Every wait
-// is bounded; on expiry the kernel flags the device status word, drains
-// in-flight copies and MMAs, frees TMEM and returns.  A CTA leaves only after a
-// cluster barrier, so no peer still writes into it.
+// Tiling.  A pair tile is 128 tokens (UMMA M) x 64 weight rows: two 32-row
+// boxes chosen so that every neox pair lands in one thread — for a q or k tile
+// rows (h*hd + d0 .. +31) and (h*hd + hd/2 + d0 .. +31), for a v tile 64
+// consecutive rows.  A thread-block cluster of S CTAs owns S consecutive pair
+// tiles and splits K (64-wide blocks, 128 bytes: one 128B-swizzle row) into S
+// ranges: each CTA multiplies its K range of X by the W rows of all S tiles
+// (one UMMA with N = 64 S), so it stages 1/S of X per weight row.  Warp 0 lane 0
+// streams W boxes into its ring (before the dependency wait: weights are
+// parameters), warp 2 lane 0 the X blocks into another (mbarrier transaction
+// counts); warp 1 lane 0 issues tcgen05.mma (kind::f16, bf16 x bf16 -> f32 in
+// TMEM, K = 16 per instruction) and frees stages with tcgen05.commit.  After
+// the K loop each CTA writes its partial sums of every other tile into that
+// tile's CTA (distributed shared memory), and CTA r adds the S partials of tile
+// r in rank order, so the result does not depend on which CTA finishes first.
+// All four warps then run the epilogue of tile r, one token per thread: bias,
+// RoPE, Y through shared memory (128-byte swizzle) and two TMA tensor stores,
+// the token's k/v cache rows as 16-byte stores.  Every wait is bounded; on
+// expiry the kernel flags the device status word, drains in-flight copies and
+// MMAs, frees TMEM and returns.  Cluster barriers order the exchange, and a CTA
+// leaves only after the last one, so no peer still reads or writes it.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -45,32 +45,37 @@ constexpr int kBN = 64;                        // weight rows per tile (UMMA N)
 constexpr int kBox = 32;                       // rows per W box
 constexpr int kBK = 64;                        // K per stage (bf16): 128 bytes
 constexpr int kUK = 16;                        // K per tcgen05.mma, kind::f16
-#ifndef QKV_PREFILL_KSUB
-#define QKV_PREFILL_KSUB 2
-#endif
-#ifndef QKV_PREFILL_X_STAGES
-#define QKV_PREFILL_X_STAGES 4
-#endif
-#ifndef QKV_PREFILL_W_STAGES
-#define QKV_PREFILL_W_STAGES 6
-#endif
-// A stage holds kSub consecutive 64-wide K blocks, so each weight row is
-// requested kSub * 128 contiguous bytes at a time.  X (L2-resident, shared by
-// the cluster) and W (streamed from HBM) have rings of their own: W, the long-
-// latency stream, gets the deeper one.
-constexpr int kSub = QKV_PREFILL_KSUB;
-constexpr int kXStages = QKV_PREFILL_X_STAGES;
-constexpr int kWStages = QKV_PREFILL_W_STAGES;
 constexpr int kThreads = 128;
-constexpr uint32_t kABlk = kBM * kBK * 2;      // 16 KB: one X block (128 x 64)
-constexpr uint32_t kBBlk = kBN * kBK * 2;      // 8 KB: one W block (64 x 64)
-constexpr uint32_t kABytes = kSub * kABlk;     // X bytes per stage
-constexpr uint32_t kBBytes = kSub * kBBlk;     // W bytes per stage
+constexpr uint32_t kABlk = kBM * kBK * 2;      // 16 KB: one X block (128 tokens x 64 K)
+constexpr uint32_t kTileBlk = kBN * kBK * 2;   // 8 KB: one pair tile's W block (64 rows x 64 K)
 constexpr uint32_t kBoxBytes = kBox * kBK * 2; // 4 KB
-constexpr uint32_t kTmemCols = 64;             // f32 accumulator columns (= kBN)
-constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kXStages * kABytes + kWStages * kBBytes +
-                              (2 * kXStages + 2 * kWStages + 1) * sizeof(uint64_t) + 16;
-static_assert(kSmemBytes <= 227 * 1024, "prefill rings exceed shared memory");
+constexpr size_t kRingBytes = 224 * 1024;      // X ring + W ring
+constexpr uint32_t kXchgStride = kBN + 4;      // floats per token row of an exchange slot (padded)
+constexpr uint32_t kXchgSlot = kBM * kXchgStride * 4;
+
+// Shape of a cluster of S CTAs.  The cluster owns S consecutive pair tiles
+// (64 weight rows each) and splits K in S ranges; every CTA multiplies its K
+// range of X by the S tiles' W rows (UMMA N = 64 S) and ends with partial sums
+// of all S tiles.  kSub 64-wide K blocks form a stage.
+template <int S>
+struct Split {
+    static constexpr int kN = kBN * S;                        // UMMA N and TMEM columns
+    static constexpr int kSub = S >= 4 ? 1 : 2;
+    static constexpr uint32_t kXStage = kSub * kABlk;
+    static constexpr uint32_t kWBlk = S * kTileBlk;           // W bytes of one K block
+    static constexpr uint32_t kWStage = kSub * kWBlk;
+    static constexpr int kXStages = S == 1 ? 4 : (S == 2 ? 3 : 6);
+    static constexpr int kWStages = static_cast<int>((kRingBytes - kXStages * kXStage) / kWStage);
+    static constexpr size_t kSmem = 1024 /* alignment slack */ + kXStages * kXStage + kWStages * kWStage +
+                                    (2 * kXStages + 2 * kWStages + 1) * sizeof(uint64_t) + 16;
+    static_assert(kXStages * kXStage + kWStages * kWStage <= kRingBytes, "rings");
+    static_assert(kSmem <= 227 * 1024, "prefill rings exceed shared memory");
+    // after the K loop the rings hold S exchange slots and the Y staging boxes
+    static_assert(S * kXchgSlot + 2 * kBM * kBox * 4 <= kRingBytes, "exchange space");
+    // instruction descriptor, kind::f16: D f32, A and B bf16, both K-major
+    static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                                       (static_cast<uint32_t>(kN >> 3) << 17) | ((kBM >> 4) << 24);
+};
 
 constexpr unsigned int kFlagPosRange = 1u;
 constexpr unsigned int kFlagTimeout = 2u;
@@ -91,17 +96,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
         "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// The same box into the same shared-memory offset of every CTA in `mask`; each
-// destination CTA's barrier at `bar`'s offset receives the bytes it got.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar,
-                                               uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
-        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(mask)
         : "memory");
 }
 
@@ -131,16 +125,16 @@ __device__ __forceinline__ uint32_t cluster_rank() {
     return r;
 }
 
-__device__ __forceinline__ uint32_t cluster_id_x() {
+// Shared::cluster address of `p`'s offset in the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(const void* p, uint32_t rank) {
     uint32_t r;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
     return r;
 }
 
-__device__ __forceinline__ uint32_t cluster_count_x() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-    return r;
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
 }
 
 // All threads of every CTA in the cluster; release/acquire orders shared-memory
@@ -178,19 +172,12 @@ __device__ __forceinline__ uint64_t smem_desc_k128(const void* tile) {
     return d;
 }
 
-// Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major, N = 64, M = 128.
-constexpr uint32_t kIdesc = (1u << 4)             // D format: f32
-                            | (1u << 7)           // A format: bf16
-                            | (1u << 10)          // B format: bf16
-                            | ((kBN >> 3) << 17)  // N >> 3
-                            | ((kBM >> 4) << 24); // M >> 4
-
-__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t accumulate) {
+__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "l"(da), "l"(db), "r"(kIdesc), "r"(accumulate)
+        "l"(da), "l"(db), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -198,16 +185,6 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
-}
-
-// Arrive once on the barrier at `bar`'s offset in every CTA of `mask` when the
-// MMAs issued so far have completed.
-__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(mask)
-        : "memory");
 }
 
 // 32 consecutive f32 columns of this warp's 32 TMEM lanes: thread l gets lane
@@ -232,80 +209,87 @@ __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sy
 
 // ---------------------------------------------------------------- kernel
 
+// Section and section-local first rows of pair tile `tile` (64 weight rows): for
+// a q or k tile the boxes (h*hd + d0 ..) and (h*hd + hd/2 + d0 ..), for a v tile
+// 64 consecutive rows.  `base` is the section's first global row.
+struct PairTile {
+    int sec, rowA, rowB, d0, base;
+};
+
+__device__ __forceinline__ PairTile pair_tile(int tile, const PrefillParams& p) {
+    PairTile t;
+    const int half = p.hd >> 1;
+    const int tiles_per_head = p.hd / kBN;
+    const int tq = p.nqt / kBN, tk = p.nkt / kBN;
+    if (tile < tq + tk) {
+        t.sec = tile < tq ? 0 : 1;
+        const int v = t.sec ? tile - tq : tile;
+        const int h = v / tiles_per_head;
+        t.d0 = (v - h * tiles_per_head) * kBox;
+        t.rowA = h * p.hd + t.d0;
+        t.rowB = t.rowA + half;
+    } else {
+        t.sec = 2;
+        t.d0 = 0;
+        t.rowA = (tile - tq - tk) * kBN;
+        t.rowB = t.rowA + kBox;
+    }
+    t.base = t.sec == 0 ? 0 : (t.sec == 1 ? p.nqt : p.nqt + p.nkt);
+    return t;
+}
+
+template <int S>
 __global__ void __launch_bounds__(kThreads, 1)
     qkv_prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-                       const __grid_constant__ CUtensorMap tm_y, const __grid_constant__ PrefillParams p, int cn) {
+                       const __grid_constant__ CUtensorMap tm_y, const __grid_constant__ PrefillParams p) {
+    using C = Split<S>;
     extern __shared__ unsigned char smem_raw[];
     __shared__ float bias_s[kBN];
     __shared__ float freq_s[kBox];
     __shared__ uint32_t tmem_slot;
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    unsigned char* sA = smem;                          // X ring
-    unsigned char* sB = smem + kXStages * kABytes;     // W ring
-    uint64_t* xfull = reinterpret_cast<uint64_t*>(sB + kWStages * kBBytes);
-    uint64_t* xempty = xfull + kXStages;
-    uint64_t* wfull = xempty + kXStages;
-    uint64_t* wempty = wfull + kWStages;
-    uint64_t* done = wempty + kWStages;
+    unsigned char* sA = smem;                              // X ring
+    unsigned char* sB = smem + C::kXStages * C::kXStage;   // W ring
+    uint64_t* xfull = reinterpret_cast<uint64_t*>(sB + C::kWStages * C::kWStage);
+    uint64_t* xempty = xfull + C::kXStages;
+    uint64_t* wfull = xempty + C::kXStages;
+    uint64_t* wempty = wfull + C::kWStages;
+    uint64_t* done = wempty + C::kWStages;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.y * kBM;
-    const int half = p.hd >> 1;
-    const int tiles_per_head = p.hd / kBN;
-    const int tq = p.nqt / kBN, tk = p.nkt / kBN;
-    const int tile = blockIdx.x;
-    int sec, rowA, rowB, d0;  // section and section-local first rows of the two boxes
-    if (tile < tq + tk) {
-        sec = tile < tq ? 0 : 1;
-        const int v = sec ? tile - tq : tile;
-        const int h = v / tiles_per_head;
-        d0 = (v - h * tiles_per_head) * kBox;
-        rowA = h * p.hd + d0;
-        rowB = rowA + half;
-    } else {
-        sec = 2;
-        d0 = 0;
-        rowA = (tile - tq - tk) * kBN;
-        rowB = rowA + kBox;
-    }
-    const int base = sec == 0 ? 0 : (sec == 1 ? p.nqt : p.nqt + p.nkt);  // section's first global row
-    const int nk = (p.H + kSub * kBK - 1) / (kSub * kBK);  // stages of kSub K blocks
-    // Clusters start their K loop at different blocks, so the X tiles read at any
-    // moment are spread over L2; the CTAs of one cluster share X and move together.
-#ifndef QKV_PREFILL_STAGGER
-#define QKV_PREFILL_STAGGER 1
-#endif
-    const int k_first =
-        QKV_PREFILL_STAGGER ? static_cast<int>((static_cast<long long>(cluster_id_x()) * nk) / cluster_count_x()) : 0;
-    const uint32_t rank = cluster_rank();
-    const uint16_t cmask = static_cast<uint16_t>((1u << cn) - 1u);
-    const int slice = kBM / cn;  // X rows this CTA loads (and multicasts) per block
+    const uint32_t rank = S > 1 ? cluster_rank() : 0u;
+    // this CTA's K range, in 64-wide blocks, and the pair tiles of its cluster
+    const int nkb = (p.H + kBK - 1) / kBK;
+    const int kb_lo = static_cast<int>(rank) * nkb / S, kb_hi = (static_cast<int>(rank) + 1) * nkb / S;
+    const int n_stages = (kb_hi - kb_lo + C::kSub - 1) / C::kSub;
+    const int tile0 = (blockIdx.x / S) * S;  // first pair tile of the cluster
+    const PairTile own = pair_tile(tile0 + static_cast<int>(rank), p);  // the tile this CTA finishes
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(&tmem_slot)),
-                     "r"(kTmemCols)
+                     "r"(static_cast<uint32_t>(C::kN))
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (threadIdx.x == 32) {
-        for (int s = 0; s < kXStages; ++s) {
+        for (int s = 0; s < C::kXStages; ++s) {
             mbar_init(&xfull[s], 1);
-            mbar_init(&xempty[s], static_cast<uint32_t>(cn));  // one release from each CTA of the cluster
+            mbar_init(&xempty[s], 1);
         }
-        for (int s = 0; s < kWStages; ++s) {
+        for (int s = 0; s < C::kWStages; ++s) {
             mbar_init(&wfull[s], 1);
             mbar_init(&wempty[s], 1);
         }
         mbar_init(done, 1);
         mbar_fence_init();
     }
-    if (threadIdx.x < kBox) bias_s[threadIdx.x] = p.bias[base + rowA + threadIdx.x];
-    else if (threadIdx.x < 2 * kBox) bias_s[threadIdx.x] = p.bias[base + rowB + threadIdx.x - kBox];
-    else if (threadIdx.x < 3 * kBox && sec < 2) freq_s[threadIdx.x - 2 * kBox] = p.inv_freq[d0 + threadIdx.x - 2 * kBox];
+    if (threadIdx.x < kBox) bias_s[threadIdx.x] = p.bias[own.base + own.rowA + threadIdx.x];
+    else if (threadIdx.x < 2 * kBox) bias_s[threadIdx.x] = p.bias[own.base + own.rowB + threadIdx.x - kBox];
+    else if (threadIdx.x < 3 * kBox && own.sec < 2) freq_s[threadIdx.x - 2 * kBox] = p.inv_freq[own.d0 + threadIdx.x - 2 * kBox];
     tc_fence_before();
-    // every barrier of the cluster is initialised before any peer copies or commits to it
     cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
@@ -317,115 +301,146 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!(warp == 0 && lane == 0)) griddep_wait();
 
     if (warp == 0 && lane == 0) {
-        // ---- W producer: two 32 x 64 boxes per K block, local ring ----
+        // ---- W producer: per K block, the two 32-row boxes of each of the S pair tiles ----
         prefetch_tensormap(&tm_w);
         int issued = 0;
-        for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % kWStages;
-            if (kb >= kWStages && !mbar_wait_bounded(&wempty[s], ((kb / kWStages) - 1) & 1)) {
+        for (int st = 0; st < n_stages; ++st) {
+            const int s = st % C::kWStages;
+            if (st >= C::kWStages && !mbar_wait_bounded(&wempty[s], ((st / C::kWStages) - 1) & 1)) {
                 flag_timeout();
                 break;
             }
-            const int kx = (k_first + kb) % nk;  // stage index along K
-            mbar_arrive_expect_tx(&wfull[s], kBBytes);
+            const int kb0 = kb_lo + st * C::kSub;
+            const int valid = min(C::kSub, kb_hi - kb0);
+            mbar_arrive_expect_tx(&wfull[s], static_cast<uint32_t>(valid) * C::kWBlk);
+            for (int j = 0; j < valid; ++j) {
+                const int kc = (kb0 + j) * kBK;
 #pragma unroll
-            for (int j = 0; j < kSub; ++j) {
-                const int kc = (kx * kSub + j) * kBK;  // element column of this 64-wide block
-                unsigned char* b = sB + s * kBBytes + j * kBBlk;
-                tma_load_2d(b, &tm_w, kc, base + rowA, &wfull[s]);
-                tma_load_2d(b + kBoxBytes, &tm_w, kc, base + rowB, &wfull[s]);
+                for (int t = 0; t < S; ++t) {
+                    const PairTile pt = pair_tile(tile0 + t, p);
+                    unsigned char* b = sB + s * C::kWStage + j * C::kWBlk + t * kTileBlk;
+                    tma_load_2d(b, &tm_w, kc, pt.base + pt.rowA, &wfull[s]);
+                    tma_load_2d(b + kBoxBytes, &tm_w, kc, pt.base + pt.rowB, &wfull[s]);
+                }
             }
             ++issued;
         }
         // Drain: every W copy has landed and the MMAs released the last stages.
-        const int first = issued > kWStages ? issued - kWStages : 0;
-        for (int kb = first; kb < issued; ++kb) {
-            if (!mbar_wait_bounded(&wfull[kb % kWStages], (kb / kWStages) & 1)) flag_timeout();
-            if (!mbar_wait_bounded(&wempty[kb % kWStages], (kb / kWStages) & 1)) flag_timeout();
+        const int first = issued > C::kWStages ? issued - C::kWStages : 0;
+        for (int st = first; st < issued; ++st) {
+            if (!mbar_wait_bounded(&wfull[st % C::kWStages], (st / C::kWStages) & 1)) flag_timeout();
+            if (!mbar_wait_bounded(&wempty[st % C::kWStages], (st / C::kWStages) & 1)) flag_timeout();
         }
         griddep_wait();  // before this thread writes its epilogue rows
     } else if (warp == 2 && lane == 0) {
-        // ---- X producer: this CTA's slice of each 128 x 64 X block, multicast to the cluster ----
+        // ---- X producer: 128 x 64 X blocks of this CTA's K range ----
         prefetch_tensormap(&tm_x);
         int issued = 0;
-        for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % kXStages;
-            if (kb >= kXStages && !mbar_wait_bounded(&xempty[s], ((kb / kXStages) - 1) & 1)) {
+        for (int st = 0; st < n_stages; ++st) {
+            const int s = st % C::kXStages;
+            if (st >= C::kXStages && !mbar_wait_bounded(&xempty[s], ((st / C::kXStages) - 1) & 1)) {
                 flag_timeout();
                 break;
             }
-            const int kx = (k_first + kb) % nk;
-            mbar_arrive_expect_tx(&xfull[s], kABytes);  // the whole block: every CTA's slice lands here
-#pragma unroll
-            for (int j = 0; j < kSub; ++j) {
-                unsigned char* a = sA + s * kABytes + j * kABlk + static_cast<uint32_t>(rank) * slice * (kBK * 2);
-                const int kc = (kx * kSub + j) * kBK;
-                if (cn == 1)
-                    tma_load_2d(a, &tm_x, kc, m0, &xfull[s]);
-                else
-                    tma_load_2d_mc(a, &tm_x, kc, m0 + static_cast<int>(rank) * slice, &xfull[s], cmask);
-            }
+            const int kb0 = kb_lo + st * C::kSub;
+            const int valid = min(C::kSub, kb_hi - kb0);
+            mbar_arrive_expect_tx(&xfull[s], static_cast<uint32_t>(valid) * kABlk);
+            for (int j = 0; j < valid; ++j)
+                tma_load_2d(sA + s * C::kXStage + j * kABlk, &tm_x, (kb0 + j) * kBK, m0, &xfull[s]);
             ++issued;
         }
-        // Drain: every slice into this CTA (its own and its peers') has landed, and
-        // every CTA of the cluster released the last stages, so no peer commit is
-        // still on its way to these barriers.
-        const int first = issued > kXStages ? issued - kXStages : 0;
-        for (int kb = first; kb < issued; ++kb) {
-            if (!mbar_wait_bounded(&xfull[kb % kXStages], (kb / kXStages) & 1)) flag_timeout();
-            if (!mbar_wait_bounded(&xempty[kb % kXStages], (kb / kXStages) & 1)) flag_timeout();
+        const int first = issued > C::kXStages ? issued - C::kXStages : 0;
+        for (int st = first; st < issued; ++st) {
+            if (!mbar_wait_bounded(&xfull[st % C::kXStages], (st / C::kXStages) & 1)) flag_timeout();
+            if (!mbar_wait_bounded(&xempty[st % C::kXStages], (st / C::kXStages) & 1)) flag_timeout();
         }
     } else if (warp == 1 && lane == 0) {
-        // ---- MMA issuer ----
-        for (int kb = 0; kb < nk; ++kb) {
-            const int xs = kb % kXStages, ws = kb % kWStages;
-            if (!mbar_wait_bounded(&xfull[xs], (kb / kXStages) & 1) ||
-                !mbar_wait_bounded(&wfull[ws], (kb / kWStages) & 1)) {
+        // ---- MMA issuer: D[128 x 64 S] += X block * (S tiles' W block)^T ----
+        for (int st = 0; st < n_stages; ++st) {
+            const int xs = st % C::kXStages, ws = st % C::kWStages;
+            if (!mbar_wait_bounded(&xfull[xs], (st / C::kXStages) & 1) ||
+                !mbar_wait_bounded(&wfull[ws], (st / C::kWStages) & 1)) {
                 flag_timeout();
                 break;
             }
             tc_fence_after();
-#pragma unroll
-            for (int j = 0; j < kSub; ++j) {
-                const unsigned char* a = sA + xs * kABytes + j * kABlk;
-                const unsigned char* b = sB + ws * kBBytes + j * kBBlk;
+            const int valid = min(C::kSub, kb_hi - (kb_lo + st * C::kSub));
+            for (int j = 0; j < valid; ++j) {
+                const unsigned char* a = sA + xs * C::kXStage + j * kABlk;
+                const unsigned char* b = sB + ws * C::kWStage + j * C::kWBlk;
 #pragma unroll
                 for (int k = 0; k < kBK / kUK; ++k)
-                    tc_mma(tmem, smem_desc_k128(a + k * kUK * 2), smem_desc_k128(b + k * kUK * 2),
-                           (kb | j | k) != 0);
+                    tc_mma(tmem, smem_desc_k128(a + k * kUK * 2), smem_desc_k128(b + k * kUK * 2), C::kIdesc,
+                           (st | j | k) != 0);
             }
-            // Both stages are free in this CTA once these MMAs have read them; an X
-            // stage must be freed by every CTA of the cluster before a peer reloads it.
-            tc_commit(&wempty[ws]);
-            if (cn == 1)
-                tc_commit(&xempty[xs]);
-            else
-                tc_commit_mc(&xempty[xs], cmask);
+            tc_commit(&wempty[ws]);  // both stages are free once these MMAs have read them
+            tc_commit(&xempty[xs]);
         }
         tc_commit(done);  // arrives when every MMA issued above has completed
     }
     __syncwarp();
 
-    // ---- epilogue: thread (warp, lane) owns TMEM lane 32*warp + lane = token m0 + that ----
+    // ---- partial sums: thread (warp, lane) owns TMEM lane 32*warp + lane = token m0 + that ----
     // Warp-uniform: tcgen05.ld below is a warp-collective instruction.
     const bool acc_ready = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(done, 0));
     if (!acc_ready && lane == 0) flag_timeout();
     tc_fence_after();
+    const int tl = warp * 32 + lane;  // this thread's token within the tile
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    float* xchg = reinterpret_cast<float*>(smem);  // S slots of [128 tokens x kXchgStride], after the K loop
+    if constexpr (S > 1) {
+        // Every CTA of the cluster is past its K loop before any ring is overwritten.
+        tc_fence_before();
+        cluster_sync_all();
+        tc_fence_after();
+        if (acc_ready) {
+            // Send this CTA's partial sums of tile q to CTA q, into slot `rank` there.
+#pragma unroll 1
+            for (int q = 0; q < S; ++q) {
+                if (q == static_cast<int>(rank)) continue;
+                float v[kBN];
+                tc_ld_32cols(taddr + q * kBN, v);
+                tc_ld_32cols(taddr + q * kBN + kBox, v + kBox);
+                tc_wait_ld();
+                const uint32_t dst = map_to_rank(xchg + (rank * kBM + tl) * kXchgStride, static_cast<uint32_t>(q));
+#pragma unroll
+                for (int c = 0; c < kBN; c += 4) st_cluster_v4(dst + c * 4, v[c], v[c + 1], v[c + 2], v[c + 3]);
+            }
+        }
+        // The partial sums of every peer have landed in this CTA's slots.
+        cluster_sync_all();
+    }
     float acc[kBN];
     if (acc_ready) {
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        tc_ld_32cols(taddr, acc);
-        tc_ld_32cols(taddr + kBox, acc + kBox);
+        tc_ld_32cols(taddr + rank * kBN, acc);
+        tc_ld_32cols(taddr + rank * kBN + kBox, acc + kBox);
         tc_wait_ld();
+        if constexpr (S > 1) {
+            // Sum the S K ranges in rank order (the same order in every CTA).
+            float sum[kBN];
+            const float* s0 = xchg + tl * kXchgStride;
+#pragma unroll
+            for (int c = 0; c < kBN; ++c) sum[c] = rank == 0 ? acc[c] : s0[c];
+#pragma unroll 1
+            for (int q = 1; q < S; ++q) {
+                const float* sq = xchg + (q * kBM + tl) * kXchgStride;
+#pragma unroll
+                for (int c = 0; c < kBN; ++c) sum[c] = __fadd_rn(sum[c], q == static_cast<int>(rank) ? acc[c] : sq[c]);
+            }
+#pragma unroll
+            for (int c = 0; c < kBN; ++c) acc[c] = sum[c];
+        }
     }
-    const int tl = warp * 32 + lane;  // this thread's token within the tile
+
+    // ---- epilogue of this CTA's tile ----
     const int t = m0 + tl;
+    float* ys = xchg + S * (kXchgSlot / 4);  // Y staging, past the exchange slots
     if (acc_ready) {
         const bool live = t < p.nt;
         const int pos = live ? p.positions[t] : 0;
         const bool store = live && pos_ok(pos, p.n_ctx);
         if (live && !store) flag_bad_pos(pos);
-        if (sec < 2) {
+        if (own.sec < 2) {
 #pragma unroll
             for (int i = 0; i < kBox; ++i) {
                 const float x0 = __fadd_rn(acc[i], bias_s[i]);
@@ -439,9 +454,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < kBN; ++i) acc[i] = __fadd_rn(acc[i], bias_s[i]);
         }
-        // Y: stage both 32-column boxes in the (now idle) ring, row tl of each box,
-        // in the 128-byte-swizzled layout the Y tensor map stores from.
-        float* ys = reinterpret_cast<float*>(smem);
+        // Y: stage both 32-column boxes, row tl of each box, in the 128-byte-swizzled
+        // layout the Y tensor map stores from.
 #pragma unroll
         for (int c = 0; c < kBox / 4; ++c) {
             const int sw = (c ^ (tl & 7)) * 4;
@@ -451,9 +465,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 make_float4(acc[kBox + 4 * c], acc[kBox + 4 * c + 1], acc[kBox + 4 * c + 2], acc[kBox + 4 * c + 3]);
         }
         // k and v rows of the cache: 16-byte stores of this token's two 32-column runs.
-        if (store && sec > 0) {
+        if (store && own.sec > 0) {
             const size_t kvrow = static_cast<size_t>(pos) * static_cast<size_t>(p.nkt);
-            void* kv = sec == 1 ? p.kv_k : p.kv_v;
+            void* kv = own.sec == 1 ? p.kv_k : p.kv_v;
             if (p.kv_f16) {
                 __half* dst = static_cast<__half*>(kv) + kvrow;
 #pragma unroll
@@ -469,16 +483,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc[kBox + 8 * c + 2 * e + 1])))
                                  << 16);
                     }
-                    *reinterpret_cast<uint4*>(dst + rowA + 8 * c) = ua;
-                    *reinterpret_cast<uint4*>(dst + rowB + 8 * c) = ub;
+                    *reinterpret_cast<uint4*>(dst + own.rowA + 8 * c) = ua;
+                    *reinterpret_cast<uint4*>(dst + own.rowB + 8 * c) = ub;
                 }
             } else {
                 float* dst = static_cast<float*>(kv) + kvrow;
 #pragma unroll
                 for (int c = 0; c < kBox / 4; ++c) {
-                    *reinterpret_cast<float4*>(dst + rowA + 4 * c) =
+                    *reinterpret_cast<float4*>(dst + own.rowA + 4 * c) =
                         make_float4(acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
-                    *reinterpret_cast<float4*>(dst + rowB + 4 * c) = make_float4(
+                    *reinterpret_cast<float4*>(dst + own.rowB + 4 * c) = make_float4(
                         acc[kBox + 4 * c], acc[kBox + 4 * c + 1], acc[kBox + 4 * c + 2], acc[kBox + 4 * c + 3]);
                 }
             }
@@ -488,20 +502,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Every warp has staged its rows (or the accumulator never became ready).
     const bool tile_ready = __syncthreads_and(acc_ready) != 0;
     if (tile_ready && threadIdx.x == 0) {
-        const float* ys = reinterpret_cast<const float*>(smem);
-        tma_store_2d(&tm_y, ys, base + rowA, m0);
-        tma_store_2d(&tm_y, ys + kBM * kBox, base + rowB, m0);
+        tma_store_2d(&tm_y, ys, own.base + own.rowA, m0);
+        tma_store_2d(&tm_y, ys + kBM * kBox, own.base + own.rowB, m0);
         bulk_commit_and_wait_read();  // the boxes are read out before the CTA lets go of its shared memory
     }
     tc_fence_before();
-    // No CTA leaves while a peer of its cluster may still write into it.
+    // No CTA leaves while a peer of its cluster may still read or write it.
     cluster_sync_all();
     if (warp == 0) {
         // After a timeout, give in-flight MMAs a second bounded wait before the
         // accumulator columns are released.
         if (!acc_ready) mbar_wait_bounded(done, 0);
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(static_cast<uint32_t>(C::kN))
                      : "memory");
     }
 }
@@ -551,6 +565,34 @@ bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 
 }  // namespace
 
+namespace {
+
+template <int S>
+cudaError_t launch_split(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const CUtensorMap& tm_y,
+                         const PrefillParams& p, int tiles, bool pdl, cudaStream_t stream) {
+    auto kernel = qkv_prefill_kernel<S>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(Split<S>::kSmem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tiles, (p.nt + kBM - 1) / kBM);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Split<S>::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kernel, tm_x, tm_w, tm_y, p);
+}
+
+}  // namespace
+
 qkv_status launch_prefill(const PrefillParams& p, bool pdl, cudaStream_t stream, const char** why) {
     if (p.hd % kBN != 0) {
         *why = "head_dim must be a multiple of 64 (two 32-row boxes per neox tile)";
@@ -574,41 +616,28 @@ qkv_status launch_prefill(const PrefillParams& p, bool pdl, cudaStream_t stream,
     }
     const int R = p.nqt + 2 * p.nkt;
     const int tiles = R / kBN;
-    // Cluster of CN consecutive row tiles sharing X: the largest of 4, 2, 1 that divides the tiles.
-#ifndef QKV_PREFILL_CLUSTER
-#define QKV_PREFILL_CLUSTER 4
+    // Cluster of S pair tiles splitting K: the largest of 4, 2, 1 that divides the
+    // tiles and leaves every CTA at least one 64-wide K block.
+#ifndef QKV_PREFILL_SPLIT
+#define QKV_PREFILL_SPLIT 2
 #endif
-    int cn = QKV_PREFILL_CLUSTER;
-    while (cn > 1 && tiles % cn != 0) cn >>= 1;
+    const int nkb = (p.H + kBK - 1) / kBK;
+    int split = QKV_PREFILL_SPLIT;
+    while (split > 1 && (tiles % split != 0 || nkb < split)) split >>= 1;
     CUtensorMap tm_x, tm_w, tm_y;
     if (!encode_f32_2d_store(&tm_y, p.Y, static_cast<uint64_t>(p.nt), static_cast<uint64_t>(R), kBM) ||
-        !encode_bf16_2d(&tm_x, p.X, static_cast<uint64_t>(p.nt), static_cast<uint64_t>(p.H),
-                        static_cast<uint32_t>(kBM / cn)) ||
+        !encode_bf16_2d(&tm_x, p.X, static_cast<uint64_t>(p.nt), static_cast<uint64_t>(p.H), kBM) ||
         !encode_bf16_2d(&tm_w, p.W, static_cast<uint64_t>(R), static_cast<uint64_t>(p.H), kBox)) {
         *why = "cuTensorMapEncodeTiled failed or is unavailable";
         return QKV_ERR_CUDA;
     }
-    cudaError_t e = cudaFuncSetAttribute(qkv_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) {
-        *why = cudaGetErrorString(e);
-        return QKV_ERR_CUDA;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(tiles, (p.nt + kBM - 1) / kBM);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(cn);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 2 : 1;
-    e = cudaLaunchKernelEx(&cfg, qkv_prefill_kernel, tm_x, tm_w, tm_y, p, cn);
+    cudaError_t e;
+    if (split == 4)
+        e = launch_split<4>(tm_x, tm_w, tm_y, p, tiles, pdl, stream);
+    else if (split == 2)
+        e = launch_split<2>(tm_x, tm_w, tm_y, p, tiles, pdl, stream);
+    else
+        e = launch_split<1>(tm_x, tm_w, tm_y, p, tiles, pdl, stream);
     if (e != cudaSuccess) {
         *why = cudaGetErrorString(e);
         return QKV_ERR_CUDA;
