@@ -250,30 +250,126 @@ def oracle_layers_per_s(w: configs.Workload, seed: int, seconds: float, max_laye
     return done / spent, done, spent
 
 
+# ---------------------------------------------------------------- oracle on all host cores
+
+def _oracle_inputs(w, seed: int, layer: int):
+    """Seeded inputs of one layer for the oracle (not timed)."""
+    if isinstance(w, configs.FfnWorkload):
+        return (synth.ffn_weight_rows(seed, layer, 0, 2 * w.n_ff, w.hidden, w.w_dtype),
+                synth.hidden(seed, 100 + layer, 0, w.hidden))
+    return (synth.weight_rows(seed, layer, 0, w.rows, w.hidden, w.w_dtype), synth.bias(seed, layer, w.rows),
+            synth.hidden(seed, layer, w.positions[0], w.hidden))
+
+
+def _oracle_run(orc, w, layer: int, inp, kv):
+    if isinstance(w, configs.FfnWorkload):
+        orc.ffn_swiglu(inp[0], inp[1])
+        return
+    W, bias, x = inp
+    kk, vv = kv
+    a, b = w.nqt, w.nqt + w.nkt
+    if layer in w.mixed_layers:
+        orc.decode_mixed(W[:a], W[a:b], W[b:], x, bias, w.n_head, w.n_head_kv, w.head_dim, w.theta,
+                         w.freq_scale, w.positions[0], kk, vv)
+    else:
+        orc.decode(W, x, bias, w.n_head, w.n_head_kv, w.head_dim, w.theta, w.freq_scale, w.positions[0], kk, vv)
+
+
+def _oracle_worker(w, seed: int, layers, start, stop, results):
+    """One host process: generate its layers' inputs, then per round wait for the start
+    barrier and run the oracle once per layer, reporting the oracle time; a round that
+    starts with `stop` set ends the process."""
+    sys.path.insert(0, ROOT)
+    import oracle
+    orc = oracle.Oracle()
+    inputs = [_oracle_inputs(w, seed, l) for l in layers]
+    kv = None
+    if not isinstance(w, configs.FfnWorkload):
+        kk = np.zeros((w.n_ctx, w.nkt), np.float32 if w.kv_dtype == "f32" else np.uint16)
+        kv = (kk, kk.copy())
+    while True:
+        start.wait()
+        if stop.value:
+            return
+        t0 = time.perf_counter()
+        for l, inp in zip(layers, inputs):
+            _oracle_run(orc, w, l, inp, kv)
+        results.put(time.perf_counter() - t0)
+
+
+def oracle_all_cores(w, seed: int, seconds: float = 0.0, rounds: int | None = None, warmup: int = 0):
+    """Run the unmodified oracle in one spawned process per host core, all at once, one
+    layer each per round (a round is timed by its slowest process).  Runs `rounds` rounds,
+    or until about `seconds` of CPU time, after `warmup` untimed rounds.  Returns
+    (layers/s, cores, layers, seconds).  Spawned, not forked: the parent may hold a CUDA
+    context."""
+    import multiprocessing as mp
+    import oracle
+    oracle.load()  # build once here, not in every worker
+    cores = len(os.sched_getaffinity(0))
+    ctx = mp.get_context("spawn")
+    start = ctx.Barrier(cores + 1)
+    stop = ctx.Value("b", 0)
+    results = ctx.Queue()
+    procs = [ctx.Process(target=_oracle_worker, args=(w, seed, [i % w.n_layers], start, stop, results),
+                         daemon=True)
+             for i in range(cores)]
+    for pr in procs:
+        pr.start()
+    total, done, r = 0.0, 0, 0
+    try:
+        while True:
+            start.wait(timeout=180)
+            t = max(results.get(timeout=300) for _ in range(cores))
+            r += 1
+            if r > warmup:
+                total += t
+                done += 1
+            if (rounds is not None and done >= rounds) or (rounds is None and total * cores >= seconds):
+                break
+        stop.value = 1
+        start.wait(timeout=60)
+    finally:
+        for pr in procs:
+            pr.join(timeout=30)
+            if pr.is_alive():
+                pr.terminate()
+    return cores * done / total, cores, cores * done, total
+
+
+def cpu_baseline_leg(w, seed: int, seconds: float, what: str):
+    """cpu_baseline: the oracle on all host cores, with the single-thread figure beside it."""
+    v1, n1, s1 = (ffn_oracle_layers_per_s if isinstance(w, configs.FfnWorkload) else oracle_layers_per_s)(
+        w, seed, seconds / 4, max_layers=w.n_layers)
+    single = {"value": v1, "unit": "layers/s", "cores": 1,
+              "sample": "%d consecutive layers (%.1f s), one thread" % (n1, s1)}
+    try:
+        v, cores, layers, secs = oracle_all_cores(w, seed, seconds=seconds)
+    except Exception as exc:  # the pool is a baseline, never a reason to lose the GPU line
+        return dict(single, kind="oracle", note="all-core run failed: %s" % str(exc)[:120])
+    return {"value": v, "unit": "layers/s", "cores": cores, "kind": "oracle",
+            "sample": "%s: one layer per process on %d processes at once (one per host core), %d layers in "
+                      "%.2f s of wall time, about %.0f s of CPU; the C oracle as it stands (double "
+                      "accumulation), input generation excluded" % (what, cores, layers, secs, secs * cores),
+            "single_thread": single}
+
+
 def reference_arm(args, w):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    seed = 0
-    # warm-up layers, then K timed "steps" of one oracle layer each
-    for _ in range(args.warmup):
-        oracle_layers_per_s(w, seed, 0.0, max_layers=1)
-    total_layers, total_s = 0, 0.0
-    for _ in range(args.steps):
-        _, n, s = oracle_layers_per_s(w, seed, 0.0, max_layers=1)
-        total_layers += n
-        total_s += s
-    value = total_layers / total_s
+    # K timed steps after W untimed ones; a step is one oracle layer on every host core at once
+    value, cores, layers, secs = oracle_all_cores(w, 0, rounds=args.steps, warmup=args.warmup)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "layers/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded SplitMix64/Box-Muller weights, bias, x)",
         "config": workload_config(w),
-        "cpu_baseline": {"value": value, "unit": "layers/s", "cores": 1, "kind": "oracle",
-                         "sample": "%d steps x 1 layer of %s at pos %d, single-threaded C oracle "
-                                   "(double accumulation), weight generation excluded"
-                                   % (args.steps, w.name, w.positions[0])},
+        "cpu_baseline": {"value": value, "unit": "layers/s", "cores": cores, "kind": "oracle",
+                         "sample": "%d steps x %d layers of %s at pos %d (one per process, one process per "
+                                   "host core, at once), the C oracle as it stands (double accumulation), "
+                                   "input generation excluded" % (args.steps, cores, w.name, w.positions[0])},
         "e2e": {"value": value, "unit": "layers/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -351,11 +447,7 @@ def native_arm(args, w):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        v, n, s = oracle_layers_per_s(w, seed, args.cpu_seconds, max_layers=w.n_layers)
-        cpu = {"value": v, "unit": "layers/s", "cores": 1, "kind": "oracle",
-               "sample": "%d consecutive layers of %s at pos %d (%.1f s of oracle time), "
-                         "single-threaded C oracle, weight generation excluded"
-                         % (n, w.name, w.positions[0], s)}
+        cpu = cpu_baseline_leg(w, seed, args.cpu_seconds, "%s at pos %d" % (w.name, w.positions[0]))
 
     if rank == 0:
         line = {
@@ -534,10 +626,7 @@ def ffn_arm(args, w):
     peak, peak_kind = measured_peak()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        v, n, s = ffn_oracle_layers_per_s(w, seed, args.cpu_seconds, max_layers=L)
-        cpu = {"value": v, "unit": "layers/s", "cores": 1, "kind": "oracle",
-               "sample": "%d consecutive layers of %s (%.1f s of oracle time), single-threaded C oracle, "
-                         "weight generation excluded" % (n, w.name, s)}
+        cpu = cpu_baseline_leg(w, seed, args.cpu_seconds, w.name)
     if rank == 0:
         line = {
             "metric": FFN_METRIC, "value": world * L * args.steps / elapsed, "unit": "layers/s",
@@ -585,24 +674,17 @@ def ffn_reference_arm(args, w):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    seed = 0
-    for _ in range(args.warmup):
-        ffn_oracle_layers_per_s(w, seed, 0.0, max_layers=1)
-    total_layers, total_s = 0, 0.0
-    for _ in range(args.steps):
-        _, n, s = ffn_oracle_layers_per_s(w, seed, 0.0, max_layers=1)
-        total_layers += n
-        total_s += s
-    value = total_layers / total_s
+    value, cores, layers, secs = oracle_all_cores(w, 0, rounds=args.steps, warmup=args.warmup)
     line = {
         "impl": "reference", "metric": FFN_METRIC, "value": value, "unit": "layers/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded SplitMix64/Box-Muller weights and x)",
         "config": ffn_config(w),
-        "cpu_baseline": {"value": value, "unit": "layers/s", "cores": 1, "kind": "oracle",
-                         "sample": "%d steps x 1 layer of %s, single-threaded C oracle (double "
-                                   "accumulation), weight generation excluded" % (args.steps, w.name)},
+        "cpu_baseline": {"value": value, "unit": "layers/s", "cores": cores, "kind": "oracle",
+                         "sample": "%d steps x %d layers of %s (one per process, one process per host core, "
+                                   "at once), the C oracle as it stands (double accumulation), input "
+                                   "generation excluded" % (args.steps, cores, w.name)},
         "e2e": {"value": value, "unit": "layers/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
