@@ -45,7 +45,15 @@ constexpr int kBN = 64;                        // weight rows per tile (UMMA N)
 constexpr int kBox = 32;                       // rows per W box
 constexpr int kBK = 64;                        // K per stage (bf16): 128 bytes
 constexpr int kUK = 16;                        // K per tcgen05.mma, kind::f16
-constexpr int kThreads = 128;
+// The epilogue splits each tile's 32 neox pairs in kParts column parts: warps w and
+// w + 4k read the same TMEM lanes (tokens), each its own part, so the per-token work
+// of a thread shrinks kParts-fold; the extra warps idle through the K loop.
+#ifndef QKV_PREFILL_EPI_PARTS
+#define QKV_PREFILL_EPI_PARTS 4
+#endif
+constexpr int kParts = QKV_PREFILL_EPI_PARTS;
+static_assert(kParts == 1 || kParts == 2 || kParts == 4, "column parts");
+constexpr int kThreads = 128 * kParts;
 constexpr uint32_t kABlk = kBM * kBK * 2;      // 16 KB: one X block (128 tokens x 64 K)
 constexpr uint32_t kTileBlk = kBN * kBK * 2;   // 8 KB: one pair tile's W block (64 rows x 64 K)
 constexpr uint32_t kBoxBytes = kBox * kBK * 2; // 4 KB
@@ -203,6 +211,36 @@ __device__ __forceinline__ void tc_ld_32cols(uint32_t taddr, float* v) {
         : "r"(taddr));
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 16 / 8 consecutive f32 columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tc_ld_16cols(uint32_t taddr, float* v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tc_ld_8cols(uint32_t taddr, float* v) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// N (8, 16 or 32) consecutive columns.
+template <int N>
+__device__ __forceinline__ void tc_ld_cols(uint32_t taddr, float* v) {
+    if constexpr (N == 32) tc_ld_32cols(taddr, v);
+    else if constexpr (N == 16) tc_ld_16cols(taddr, v);
+    else tc_ld_8cols(taddr, v);
 }
 
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
@@ -380,13 +418,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
 
-    // ---- partial sums: thread (warp, lane) owns TMEM lane 32*warp + lane = token m0 + that ----
+    // ---- partial sums: thread (warp, lane) owns TMEM lane 32*(warp%4) + lane = token m0 + that,
+    // and pairs c0 .. c0 + kPc - 1 of the tile (columns c0.. of box A and 32 + c0.. of box B) ----
+    constexpr int kPc = kBox / kParts;
     // Warp-uniform: tcgen05.ld below is a warp-collective instruction.
     const bool acc_ready = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(done, 0));
     if (!acc_ready && lane == 0) flag_timeout();
     tc_fence_after();
-    const int tl = warp * 32 + lane;  // this thread's token within the tile
-    const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int quarter = warp & 3;
+    const int c0 = (warp >> 2) * kPc;
+    const int tl = quarter * 32 + lane;  // this thread's token within the tile
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     float* xchg = reinterpret_cast<float*>(smem);  // S slots of [128 tokens x kXchgStride], after the K loop
     if constexpr (S > 1) {
         // Every CTA of the cluster is past its K loop before any ring is overwritten.
@@ -398,37 +440,50 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
             for (int q = 0; q < S; ++q) {
                 if (q == static_cast<int>(rank)) continue;
-                float v[kBN];
-                tc_ld_32cols(taddr + q * kBN, v);
-                tc_ld_32cols(taddr + q * kBN + kBox, v + kBox);
+                float va[kPc], vb[kPc];
+                tc_ld_cols<kPc>(taddr + q * kBN + c0, va);
+                tc_ld_cols<kPc>(taddr + q * kBN + kBox + c0, vb);
                 tc_wait_ld();
                 const uint32_t dst = map_to_rank(xchg + (rank * kBM + tl) * kXchgStride, static_cast<uint32_t>(q));
 #pragma unroll
-                for (int c = 0; c < kBN; c += 4) st_cluster_v4(dst + c * 4, v[c], v[c + 1], v[c + 2], v[c + 3]);
+                for (int c = 0; c < kPc; c += 4) {
+                    st_cluster_v4(dst + (c0 + c) * 4, va[c], va[c + 1], va[c + 2], va[c + 3]);
+                    st_cluster_v4(dst + (kBox + c0 + c) * 4, vb[c], vb[c + 1], vb[c + 2], vb[c + 3]);
+                }
             }
         }
         // The partial sums of every peer have landed in this CTA's slots.
         cluster_sync_all();
     }
-    float acc[kBN];
+    float aa[kPc], ab[kPc];  // this thread's pairs: box A and box B values
     if (acc_ready) {
-        tc_ld_32cols(taddr + rank * kBN, acc);
-        tc_ld_32cols(taddr + rank * kBN + kBox, acc + kBox);
+        tc_ld_cols<kPc>(taddr + rank * kBN + c0, aa);
+        tc_ld_cols<kPc>(taddr + rank * kBN + kBox + c0, ab);
         tc_wait_ld();
         if constexpr (S > 1) {
             // Sum the S K ranges in rank order (the same order in every CTA).
-            float sum[kBN];
+            float sa[kPc], sb[kPc];
             const float* s0 = xchg + tl * kXchgStride;
 #pragma unroll
-            for (int c = 0; c < kBN; ++c) sum[c] = rank == 0 ? acc[c] : s0[c];
+            for (int c = 0; c < kPc; ++c) {
+                sa[c] = rank == 0 ? aa[c] : s0[c0 + c];
+                sb[c] = rank == 0 ? ab[c] : s0[kBox + c0 + c];
+            }
 #pragma unroll 1
             for (int q = 1; q < S; ++q) {
                 const float* sq = xchg + (q * kBM + tl) * kXchgStride;
+                const bool mine = q == static_cast<int>(rank);
 #pragma unroll
-                for (int c = 0; c < kBN; ++c) sum[c] = __fadd_rn(sum[c], q == static_cast<int>(rank) ? acc[c] : sq[c]);
+                for (int c = 0; c < kPc; ++c) {
+                    sa[c] = __fadd_rn(sa[c], mine ? aa[c] : sq[c0 + c]);
+                    sb[c] = __fadd_rn(sb[c], mine ? ab[c] : sq[kBox + c0 + c]);
+                }
             }
 #pragma unroll
-            for (int c = 0; c < kBN; ++c) acc[c] = sum[c];
+            for (int c = 0; c < kPc; ++c) {
+                aa[c] = sa[c];
+                ab[c] = sb[c];
+            }
         }
     }
 
@@ -439,61 +494,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool live = t < p.nt;
         const int pos = live ? p.positions[t] : 0;
         const bool store = live && pos_ok(pos, p.n_ctx);
-        if (live && !store) flag_bad_pos(pos);
+        if (live && !store && c0 == 0) flag_bad_pos(pos);
         if (own.sec < 2) {
 #pragma unroll
-            for (int i = 0; i < kBox; ++i) {
-                const float x0 = __fadd_rn(acc[i], bias_s[i]);
-                const float x1 = __fadd_rn(acc[kBox + i], bias_s[kBox + i]);
+            for (int i = 0; i < kPc; ++i) {
+                const float x0 = __fadd_rn(aa[i], bias_s[c0 + i]);
+                const float x1 = __fadd_rn(ab[i], bias_s[kBox + c0 + i]);
                 float r0, r1;
-                rope_rotate(x0, x1, rope_theta(pos, freq_s[i]), r0, r1);
-                acc[i] = r0;
-                acc[kBox + i] = r1;
+                rope_rotate(x0, x1, rope_theta(pos, freq_s[c0 + i]), r0, r1);
+                aa[i] = r0;
+                ab[i] = r1;
             }
         } else {
 #pragma unroll
-            for (int i = 0; i < kBN; ++i) acc[i] = __fadd_rn(acc[i], bias_s[i]);
+            for (int i = 0; i < kPc; ++i) {
+                aa[i] = __fadd_rn(aa[i], bias_s[c0 + i]);
+                ab[i] = __fadd_rn(ab[i], bias_s[kBox + c0 + i]);
+            }
         }
-        // Y: stage both 32-column boxes, row tl of each box, in the 128-byte-swizzled
-        // layout the Y tensor map stores from.
+        // Y: stage this thread's 16-byte chunks of row tl of both 32-column boxes, in the
+        // 128-byte-swizzled layout the Y tensor map stores from.
 #pragma unroll
-        for (int c = 0; c < kBox / 4; ++c) {
-            const int sw = (c ^ (tl & 7)) * 4;
-            *reinterpret_cast<float4*>(ys + tl * kBox + sw) =
-                make_float4(acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
+        for (int c = 0; c < kPc / 4; ++c) {
+            const int sw = (((c0 >> 2) + c) ^ (tl & 7)) * 4;
+            *reinterpret_cast<float4*>(ys + tl * kBox + sw) = make_float4(aa[4 * c], aa[4 * c + 1], aa[4 * c + 2], aa[4 * c + 3]);
             *reinterpret_cast<float4*>(ys + kBM * kBox + tl * kBox + sw) =
-                make_float4(acc[kBox + 4 * c], acc[kBox + 4 * c + 1], acc[kBox + 4 * c + 2], acc[kBox + 4 * c + 3]);
+                make_float4(ab[4 * c], ab[4 * c + 1], ab[4 * c + 2], ab[4 * c + 3]);
         }
-        // k and v rows of the cache: 16-byte stores of this token's two 32-column runs.
+        // k and v rows of the cache: 16-byte stores of this thread's runs of the token's row.
         if (store && own.sec > 0) {
             const size_t kvrow = static_cast<size_t>(pos) * static_cast<size_t>(p.nkt);
             void* kv = own.sec == 1 ? p.kv_k : p.kv_v;
             if (p.kv_f16) {
                 __half* dst = static_cast<__half*>(kv) + kvrow;
 #pragma unroll
-                for (int c = 0; c < kBox / 8; ++c) {
+                for (int c = 0; c < kPc / 8; ++c) {
                     uint4 ua, ub;
                     uint32_t* pa = &ua.x;
                     uint32_t* pb = &ub.x;
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        pa[e] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc[8 * c + 2 * e]))) |
-                                (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc[8 * c + 2 * e + 1]))) << 16);
-                        pb[e] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc[kBox + 8 * c + 2 * e]))) |
-                                (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc[kBox + 8 * c + 2 * e + 1])))
-                                 << 16);
+                        pa[e] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(aa[8 * c + 2 * e]))) |
+                                (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(aa[8 * c + 2 * e + 1]))) << 16);
+                        pb[e] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(ab[8 * c + 2 * e]))) |
+                                (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(ab[8 * c + 2 * e + 1]))) << 16);
                     }
-                    *reinterpret_cast<uint4*>(dst + own.rowA + 8 * c) = ua;
-                    *reinterpret_cast<uint4*>(dst + own.rowB + 8 * c) = ub;
+                    *reinterpret_cast<uint4*>(dst + own.rowA + c0 + 8 * c) = ua;
+                    *reinterpret_cast<uint4*>(dst + own.rowB + c0 + 8 * c) = ub;
                 }
             } else {
                 float* dst = static_cast<float*>(kv) + kvrow;
 #pragma unroll
-                for (int c = 0; c < kBox / 4; ++c) {
-                    *reinterpret_cast<float4*>(dst + own.rowA + 4 * c) =
-                        make_float4(acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
-                    *reinterpret_cast<float4*>(dst + own.rowB + 4 * c) = make_float4(
-                        acc[kBox + 4 * c], acc[kBox + 4 * c + 1], acc[kBox + 4 * c + 2], acc[kBox + 4 * c + 3]);
+                for (int c = 0; c < kPc / 4; ++c) {
+                    *reinterpret_cast<float4*>(dst + own.rowA + c0 + 4 * c) =
+                        make_float4(aa[4 * c], aa[4 * c + 1], aa[4 * c + 2], aa[4 * c + 3]);
+                    *reinterpret_cast<float4*>(dst + own.rowB + c0 + 4 * c) =
+                        make_float4(ab[4 * c], ab[4 * c + 1], ab[4 * c + 2], ab[4 * c + 3]);
                 }
             }
         }
