@@ -68,6 +68,7 @@ def _bind(lib):
     lib.oracle_silu.argtypes = [d]
     lib.oracle_silu.restype = d
     lib.oracle_ffn_swiglu.argtypes = [vp, i, vp, i64, i64, vp]
+    lib.oracle_rmsnorm.argtypes = [vp, vp, i64, d, vp]
     return lib
 
 
@@ -136,6 +137,15 @@ class Oracle:
         out = np.empty(R // 2, dtype=np.float32)
         self.lib.oracle_ffn_swiglu(_p(W), int(W.dtype == np.uint16), _p(x), R // 2, H, _p(out))
         return out
+
+    def rmsnorm(self, h: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
+        """x = h * w / sqrt(mean(h^2) + eps), float32 out."""
+        h = np.ascontiguousarray(h, dtype=np.float32)
+        w = np.ascontiguousarray(w, dtype=np.float32)
+        assert h.shape == w.shape and h.ndim == 1
+        x = np.empty_like(h)
+        self.lib.oracle_rmsnorm(_p(h), _p(w), h.size, float(eps), _p(x))
+        return x
 
     def token(self, y, bias, nh, nkv, hd, base, freq_scale, pos, kv_k, kv_v):
         """Epilogue for one token on a precomputed projection y (float64 [R])."""

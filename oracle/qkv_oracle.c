@@ -20,7 +20,10 @@
  *     fold", §2.2 (the FFN activation: gate and up projections of the normed
  *     hidden state, SiLU(x) = x * sigmoid(x), then the elementwise product)
  *     and §2.3 (the decode FusedFFN node: one concat gate|up weight, then the
- *     SwiGLU over the two halves of its output).
+ *     SwiGLU over the two halves of its output), and §2.3 / §3 (RmsNorm, the op
+ *     that produces the normed hidden state the projection reads; the pages
+ *     name it without its formula, so the oracle takes the plain definition
+ *     x_c = h_c * w_c / sqrt(mean(h^2) + eps)).
  *
  * Precision: everything is carried in double; results are rounded to f32 (or
  * f32 then f16) only where the stage stores them.  Readings taken where the
@@ -273,4 +276,15 @@ void oracle_ffn_swiglu(const void* W, int w_is_bf16, const float* x, int64_t nf,
         }
         out[i] = (float)(oracle_silu(g) * u);
     }
+}
+
+/* ---- RMSNorm of the hidden state (the step before the projection) --------- */
+
+/* x_c = RN_f32( h_c * w_c / sqrt( (1/H) sum_j h_j^2 + eps ) ), sums and products in
+ * double; x is rounded to f32 because the stage stages x in f32 before the projection. */
+void oracle_rmsnorm(const float* h, const float* w, int64_t H, double eps, float* x) {
+    double ss = 0.0;
+    for (int64_t c = 0; c < H; ++c) ss += (double)h[c] * (double)h[c];
+    const double inv = 1.0 / sqrt(ss / (double)H + eps);
+    for (int64_t c = 0; c < H; ++c) x[c] = (float)((double)h[c] * inv * (double)w[c]);
 }

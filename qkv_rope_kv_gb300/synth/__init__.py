@@ -32,10 +32,12 @@ T_HIDDEN = 3      # decode hidden vector x, keyed by position
 T_PREFILL_X = 4   # prefill activations X[t], keyed by token index t
 T_CANARY = 5      # KV-cache fill pattern for untouched-slot checks
 T_FFN_WEIGHT = 6  # concat w_gate|w_up rows of the FFN, keyed by global row index
+T_NORM = 7        # RMSNorm weight of the attention input, per layer
 
 W_SIGMA = 0.02
 BIAS_SIGMA = 0.1
 X_SIGMA = 1.0
+NORM_SIGMA = 0.1  # spread of the RMSNorm weight around 1
 
 _lock = threading.Lock()
 _lib = None
@@ -124,6 +126,11 @@ def ffn_weight_rows(seed: int, layer: int, row0: int, nrows: int, hidden: int, d
                     out: np.ndarray | None = None) -> np.ndarray:
     """Rows [row0, row0+nrows) of the concatenated w_gate|w_up matrix, ~N(0, 0.02)."""
     return rows(seed, T_FFN_WEIGHT, layer, row0, nrows, hidden, W_SIGMA, dtype, out)
+
+
+def norm_weight(seed: int, layer: int, h: int) -> np.ndarray:
+    """RMSNorm weight of a layer, float32, 1 + N(0, 0.1)."""
+    return (np.float32(1.0) + normal_f32(seed, T_NORM, layer, 0, h, NORM_SIGMA)).astype(np.float32)
 
 
 def bias(seed: int, layer: int, n_rows: int) -> np.ndarray:

@@ -465,4 +465,38 @@ def pin_ffn_zero_gate_and_unit_up(orc):
     assert abs(float(out[1]) - want) <= 2e-7 * want
 
 
+# ---------------------------------------------------------------- RMSNorm prologue
+
+def pin_rmsnorm_closed_forms(orc):
+    """h = 3 * ones, w = ones, eps = 0: mean(h^2) = 9, so x = 1 exactly; h = ones, eps = 3:
+    x = 1 / sqrt(1 + 3) = 0.5 exactly; h = 0: x = 0 for any eps > 0; h = [3, 4]: against mpmath."""
+    import mpmath
+    mpmath.mp.dps = 40
+    ones = np.ones(7, np.float32)
+    assert np.array_equal(orc.rmsnorm(3 * ones, ones, 0.0), ones)
+    assert np.array_equal(orc.rmsnorm(-3 * ones, ones, 0.0), -ones)
+    assert np.array_equal(orc.rmsnorm(ones, ones, 3.0), 0.5 * ones)
+    assert np.array_equal(orc.rmsnorm(np.zeros(5, np.float32), np.ones(5, np.float32), 1e-6), np.zeros(5, np.float32))
+    h = np.array([3.0, 4.0], np.float32)
+    want = [_mp_round_f32(mpmath.mpf(v) / mpmath.sqrt(mpmath.mpf(25) / 2 + mpmath.mpf("1e-6"))) for v in (3, 4)]
+    got = orc.rmsnorm(h, np.ones(2, np.float32), 1e-6)
+    assert np.all(np.abs(f32_bits(got).astype(np.int64) - f32_bits(np.array(want, np.float32)).astype(np.int64)) <= 1)
+
+
+def pin_rmsnorm_scale_and_weight(orc):
+    """With eps = 0, scaling h by a power of two leaves x unchanged bit for bit (every sum,
+    square and root scales exactly); the weight multiplies element by element."""
+    rng = np.random.default_rng(5)
+    h = rng.standard_normal(64).astype(np.float32)
+    w = np.ones(64, np.float32)
+    base = orc.rmsnorm(h, w, 0.0)
+    for k in (-3, 1, 5):
+        assert np.array_equal(orc.rmsnorm((h * np.float32(2.0 ** k)).astype(np.float32), w, 0.0), base)
+    w2 = np.arange(1, 65, dtype=np.float32) / np.float32(8)  # exact in f32
+    got = orc.rmsnorm(h, w2, 0.0).astype(np.float64)
+    assert np.allclose(got, base.astype(np.float64) * w2, rtol=2e-7, atol=0)
+    # the mean is over H: the norm of the normalised vector is sqrt(H)
+    assert abs(float(np.sqrt(np.sum(base.astype(np.float64) ** 2))) - 8.0) <= 1e-5
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

@@ -49,6 +49,14 @@ MUTANTS = {
                             "const float* ru = (const float*)W + (2 * nf - 1 - i) * H;"),
     "ffn_up_row_reversed_bf16": ("const uint16_t* ru = (const uint16_t*)W + (nf + i) * H;",
                                  "const uint16_t* ru = (const uint16_t*)W + (2 * nf - 1 - i) * H;"),
+    "rmsnorm_sum_not_mean": ("const double inv = 1.0 / sqrt(ss / (double)H + eps);",
+                             "const double inv = 1.0 / sqrt(ss + eps);"),
+    "rmsnorm_eps_outside_root": ("const double inv = 1.0 / sqrt(ss / (double)H + eps);",
+                                 "const double inv = 1.0 / (sqrt(ss / (double)H) + eps);"),
+    "rmsnorm_weight_dropped": ("x[c] = (float)((double)h[c] * inv * (double)w[c]);",
+                               "x[c] = (float)((double)h[c] * inv);"),
+    "rmsnorm_no_root": ("const double inv = 1.0 / sqrt(ss / (double)H + eps);",
+                        "const double inv = 1.0 / (ss / (double)H + eps);"),
     "ffn_drops_last_column": ("for (int64_t c = 0; c < H; ++c) {\n                g += (double)rg[c]",
                               "for (int64_t c = 0; c + 1 < H; ++c) {\n                g += (double)rg[c]"),
 }
