@@ -184,6 +184,8 @@ def build_model(w: configs.Workload, seed: int):
             d.update(w=dW, bias=db)
         layers.append(d)
         keep += [dW, db, dk, dv]
+    norms = [torch.from_numpy(synth.norm_weight(seed, l, w.hidden)).to("cuda") for l in range(L)] \
+        if w.rmsnorm else None
     layer_plans = [plans[Q.QKV_CLASS_MIXED if l in w.mixed_layers else Q.QKV_CLASS_CONCAT] for l in range(L)]
     h_in = torch.zeros(in_bytes, dtype=torch.uint8).pin_memory()
     h_in[:4].view(torch.int32)[0] = pos
@@ -191,7 +193,7 @@ def build_model(w: configs.Workload, seed: int):
     inbuf.copy_(h_in)
     h_out = torch.empty(L, w.rows, dtype=torch.float32).pin_memory()
     torch.cuda.synchronize()
-    return dict(plans=plans, layer_plans=layer_plans, layers=layers, keep=keep, inbuf=inbuf,
+    return dict(plans=plans, layer_plans=layer_plans, layers=layers, norms=norms, keep=keep, inbuf=inbuf,
                 dpos=dpos, dx=dx, dout=dout, h_in=h_in, h_out=h_out, in_bytes=in_bytes)
 
 
@@ -260,7 +262,10 @@ def oracle_layers_per_s(w: configs.Workload, seed: int, seconds: float, max_laye
         W = synth.weight_rows(seed, layer, 0, w.rows, w.hidden, w.w_dtype)
         bias = synth.bias(seed, layer, w.rows)
         x = synth.hidden(seed, layer, pos, w.hidden)
+        nw = synth.norm_weight(seed, layer, w.hidden) if w.rmsnorm else None
         t0 = time.perf_counter()
+        if nw is not None:
+            x = orc.rmsnorm(x, nw, w.rms_eps)
         if layer in w.mixed_layers:
             orc.decode_mixed(W[:a], W[a:b], W[b:], x, bias, w.n_head, w.n_head_kv, w.head_dim,
                              w.theta, w.freq_scale, pos, kk, vv)
@@ -280,14 +285,17 @@ def _oracle_inputs(w, seed: int, layer: int):
         return (synth.ffn_weight_rows(seed, layer, 0, 2 * w.n_ff, w.hidden, w.w_dtype),
                 synth.hidden(seed, 100 + layer, 0, w.hidden))
     return (synth.weight_rows(seed, layer, 0, w.rows, w.hidden, w.w_dtype), synth.bias(seed, layer, w.rows),
-            synth.hidden(seed, layer, w.positions[0], w.hidden))
+            synth.hidden(seed, layer, w.positions[0], w.hidden),
+            synth.norm_weight(seed, layer, w.hidden) if w.rmsnorm else None)
 
 
 def _oracle_run(orc, w, layer: int, inp, kv):
     if isinstance(w, configs.FfnWorkload):
         orc.ffn_swiglu(inp[0], inp[1])
         return
-    W, bias, x = inp
+    W, bias, x, nw = inp
+    if nw is not None:
+        x = orc.rmsnorm(x, nw, w.rms_eps)
     kk, vv = kv
     a, b = w.nqt, w.nqt + w.nkt
     if layer in w.mixed_layers:
@@ -402,6 +410,7 @@ def workload_config(w: configs.Workload):
             "heads": "%d/%d" % (w.n_head, w.n_head_kv), "head_dim": w.head_dim,
             "w_dtype": w.w_dtype, "kv_dtype": w.kv_dtype, "n_ctx": w.n_ctx, "pos": w.positions[0],
             "mixed_layers": "%d-%d" % (w.mixed_layers[0], w.mixed_layers[-1]) if w.mixed_layers else "none",
+            "rmsnorm": ("fused in front of each projection, eps %g" % w.rms_eps) if w.rmsnorm else "none (x given)",
             "l2": ("inputs larger than L2: %.2f GB of weights per step" % (w.n_layers * w.w_bytes() / 1e9))
             if w.n_layers * w.w_bytes() > 4 * L2_BYTES
             else "L2 flushed before every timed step (256 MB written outside the timed events); "
@@ -426,7 +435,11 @@ def native_arm(args, w):
     seed = rank  # each replica runs its own seeded model
     m = build_model(w, seed)
     stream = torch.cuda.Stream()
-    graph = Q.qkv_model_graph_create(m["layer_plans"], m["layers"], m["dpos"], stream)
+    if w.rmsnorm:
+        graph = Q.qkv_model_graph_create_rmsnorm(m["layer_plans"], m["layers"], m["norms"], w.rms_eps, m["dpos"],
+                                                 stream)
+    else:
+        graph = Q.qkv_model_graph_create(m["layer_plans"], m["layers"], m["dpos"], stream)
     kernels = graph.kernel_count
 
     for _ in range(max(args.warmup, 3)):

@@ -148,6 +148,26 @@ qkv_status qkv_decode_step(const qkv_plan* plan, const float* x, const void* w,
                            const float* bias, const int32_t* d_pos, float* q, float* k,
                            float* v, void* kv_k, void* kv_v, void* stream);
 
+/* As qkv_decode_step, with the layer's RMSNorm in front (the step that produces
+ * the normed hidden state the projection reads; the pages name the RmsNorm op
+ * — "06 · Assign + fusion — every node picks an engine, then patterns fold",
+ * §2.3 and §3 — without its formula, so this takes the plain definition):
+ *   x_c = (h_c * inv) * norm_w[c],  inv = 1 / sqrt(sum_j h_j^2 / H + norm_eps),
+ * computed in f32 inside the projection kernel (every CTA reduces sum(h^2) in a
+ * fixed order), then y = W x as in qkv_decode_step.
+ *   h       device, H floats: the hidden state before the norm.
+ *   norm_w  device, H floats, 16-byte aligned.
+ *   norm_eps >= 0 (Qwen2.5: 1e-6).
+ * The kernel applies the scalar 1/rms to the dot products (it commutes with the
+ * projection) and stages h * norm_w, so the sum of squares runs beside the
+ * staging; the rounding order differs from normalising first by f32 ulps.
+ * Errors: INVALID_ARG (null or misaligned norm_w, negative or NaN eps, mixed-class plan),
+ * CUDA. */
+qkv_status qkv_decode_step_rmsnorm(const qkv_plan* plan, const float* h, const float* norm_w,
+                                   float norm_eps, const void* w, const float* bias,
+                                   const int32_t* d_pos, float* q, float* k, float* v, void* kv_k,
+                                   void* kv_v, void* stream);
+
 /* Mixed class, one launch: the three projections wq (nqt x H), wk (nkt x H),
  * wv (nkt x H) and the same epilogue ("73 · D3-8 ...", §1 second complication,
  * §3.1: three matmuls without bias + one epilogue, section pointers passed in).
@@ -244,6 +264,16 @@ typedef struct qkv_graph qkv_graph;
 qkv_status qkv_model_graph_create(const qkv_plan* const* plans, int32_t n_layers,
                                   const qkv_layer_ptrs* layers, const int32_t* d_pos,
                                   void* stream, qkv_graph** out);
+/* As qkv_model_graph_create, with each layer's RMSNorm fused in front of its
+ * projection (see qkv_decode_step_rmsnorm): layers[i].x is the hidden state
+ * before the norm and norm_w[i] (device, H floats, 16-byte aligned) the layer's
+ * norm weight.
+ * Errors as qkv_model_graph_create, and INVALID_ARG for a null norm weight or
+ * a negative / NaN eps. */
+qkv_status qkv_model_graph_create_rmsnorm(const qkv_plan* const* plans, int32_t n_layers,
+                                          const qkv_layer_ptrs* layers, const float* const* norm_w,
+                                          float norm_eps, const int32_t* d_pos, void* stream,
+                                          qkv_graph** out);
 /* One decode step of the whole model: one cudaGraphLaunch on `stream`. */
 qkv_status qkv_model_graph_launch(qkv_graph* graph, void* stream);
 /* Copy-in, replay, copy-out on `stream`, for callers holding host buffers:

@@ -112,6 +112,8 @@ def _declare(lib):
         "qkv_plan_inv_freq": ([vp, vp, i32], st),
         "qkv_decode_step": ([vp] * 10 + [vp], st),
         "qkv_decode_step_mixed": ([vp] * 15, st),
+        "qkv_decode_step_rmsnorm": ([vp, vp, vp, ctypes.c_float] + [vp] * 9, st),
+        "qkv_model_graph_create_rmsnorm": ([vp, i32, vp, vp, ctypes.c_float, vp, vp, ctypes.POINTER(vp)], st),
         "qkv_project": ([vp] * 9, st),
         "qkv_epilogue": ([vp] * 11, st),
         "qkv_chain_add_bias": ([vp, vp, i64, vp], st),
@@ -213,6 +215,14 @@ def qkv_decode_step(plan: Plan, x, w, bias, d_pos, q, k, v, kv_k, kv_v, stream=N
                                 _ptr(k), _ptr(v), _ptr(kv_k), _ptr(kv_v), _stream(stream)))
 
 
+def qkv_decode_step_rmsnorm(plan: Plan, h, norm_w, norm_eps: float, w, bias, d_pos, q, k, v, kv_k, kv_v,
+                            stream=None):
+    """qkv_decode_step on RMSNorm(h) with weight norm_w, the norm computed in the kernel."""
+    _check(_lib.qkv_decode_step_rmsnorm(plan.handle, _ptr(h), _ptr(norm_w), float(norm_eps), _ptr(w), _ptr(bias),
+                                        _ptr(d_pos), _ptr(q), _ptr(k), _ptr(v), _ptr(kv_k), _ptr(kv_v),
+                                        _stream(stream)))
+
+
 def qkv_decode_step_mixed(plan: Plan, x, wq, wk, wv, bias_q, bias_k, bias_v, d_pos, q, k, v,
                           kv_k, kv_v, stream=None):
     _check(_lib.qkv_decode_step_mixed(plan.handle, _ptr(x), _ptr(wq), _ptr(wk), _ptr(wv),
@@ -303,6 +313,23 @@ def qkv_model_graph_create(plans, layers, d_pos, stream) -> ModelGraph:
     _check(_lib.qkv_model_graph_create(arr_plans, n, arr_layers, _ptr(d_pos), _stream(stream),
                                        ctypes.byref(h)))
     return ModelGraph(h.value, (plans, layers, d_pos))
+
+
+def qkv_model_graph_create_rmsnorm(plans, layers, norm_w, norm_eps: float, d_pos, stream) -> ModelGraph:
+    """As qkv_model_graph_create with each layer's RMSNorm fused in front: layers[i]["x"] is
+    the hidden state before the norm, norm_w[i] the layer's norm weight (device tensors)."""
+    n = len(plans)
+    assert len(layers) == n and len(norm_w) == n
+    arr_plans = (ctypes.c_void_p * n)(*[p.handle for p in plans])
+    arr_layers = (qkv_layer_ptrs * n)()
+    for i, L in enumerate(layers):
+        for name, _ in qkv_layer_ptrs._fields_:
+            setattr(arr_layers[i], name, _ptr(L.get(name)))
+    arr_norm = (ctypes.c_void_p * n)(*[_ptr(t) for t in norm_w])
+    h = ctypes.c_void_p()
+    _check(_lib.qkv_model_graph_create_rmsnorm(arr_plans, n, arr_layers, arr_norm, float(norm_eps), _ptr(d_pos),
+                                               _stream(stream), ctypes.byref(h)))
+    return ModelGraph(h.value, (plans, layers, norm_w, d_pos))
 
 
 def qkv_prefill_graph_create(plans, layers, nt: int, stream) -> ModelGraph:

@@ -27,6 +27,8 @@ class Workload:
     theta: float = 1.0e6
     freq_scale: float = 1.0
     nt: int = 1             # tokens per step (prefill when > 1)
+    rmsnorm: bool = False   # decode input is the hidden state; its RMSNorm runs in the projection kernel
+    rms_eps: float = 1.0e-6
 
     @property
     def nqt(self) -> int:
@@ -49,7 +51,7 @@ class Workload:
     def algo_bytes_per_layer(self) -> int:
         """Bytes one decode layer must move: W, x, bias read; q|k|v and one cache row per region written."""
         return (self.w_bytes() + 4 * self.hidden + 4 * self.rows + 4 * self.rows
-                + 2 * self.nkt * self.kv_elem_bytes())
+                + 2 * self.nkt * self.kv_elem_bytes() + (4 * self.hidden if self.rmsnorm else 0))
 
 
 QWEN05_SINGLE = Workload("qwen2.5-0.5b-single-layer", 896, 14, 2, 64, "f32", "f32", 512, 1, (17,))
@@ -61,7 +63,15 @@ QWEN14B = Workload("qwen2.5-14b-48layer-mixed", 5120, 40, 8, 128, "bf16", "f16",
 QWEN14B_PREFILL = Workload("qwen2.5-14b-prefill-nt128", 5120, 40, 8, 128, "bf16", "f16", 4096, 48,
                            tuple(range(128)), nt=128)
 
-WORKLOADS = {w.name: w for w in (QWEN05_SINGLE, QWEN05_SWEEP, QWEN7B, QWEN14B, QWEN14B_PREFILL)}
+# The same decode steps with each layer's RMSNorm fused in front (eps 1e-6, the public
+# Qwen2.5 configuration; the pages give no value).
+QWEN7B_NORM = Workload("qwen2.5-7b-28layer-rmsnorm", 3584, 28, 4, 128, "bf16", "f16", 4096, 28, (1641,),
+                       rmsnorm=True)
+QWEN14B_NORM = Workload("qwen2.5-14b-48layer-mixed-rmsnorm", 5120, 40, 8, 128, "bf16", "f16", 4096, 48, (3254,),
+                        mixed_layers=tuple(range(24, 48)), rmsnorm=True)
+
+WORKLOADS = {w.name: w for w in (QWEN05_SINGLE, QWEN05_SWEEP, QWEN7B, QWEN14B, QWEN14B_PREFILL, QWEN7B_NORM,
+                                 QWEN14B_NORM)}
 
 
 @dataclass(frozen=True)

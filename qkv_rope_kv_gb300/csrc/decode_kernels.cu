@@ -235,25 +235,107 @@ __device__ __forceinline__ void dot2_scalar(const WT* row0, const WT* row1, cons
 }
 
 // Stage x (and the frequency table) in shared memory.
+// Stage the projection input x in shared memory, threads tid = 0 .. nthr-1: bf16 rows
+// get two float4 planes (x[8c..8c+3] at c, x[8c+4..8c+7] at nch + c), aligned f32
+// rows x in order, unaligned rows scalars.  The caller synchronises before reading.
 template <typename WT, bool VEC>
-__device__ __forceinline__ void stage_x(const DecodeParams& p, float4* xs4, float* freq_s) {
+__device__ __forceinline__ void stage_plain(const DecodeParams& p, float4* xs4, int tid, int nthr) {
     const int H = p.H;
     if constexpr (VEC && sizeof(WT) == 2) {
         const int nch = H / 8;
         const float4* xg = reinterpret_cast<const float4*>(p.x);
-        for (int c = threadIdx.x; c < nch; c += blockDim.x) {
+        for (int c = tid; c < nch; c += nthr) {
             xs4[c] = xg[2 * c];
             xs4[nch + c] = xg[2 * c + 1];
         }
     } else if constexpr (VEC) {
         const int nch = H / 4;
         const float4* xg = reinterpret_cast<const float4*>(p.x);
-        for (int c = threadIdx.x; c < nch; c += blockDim.x) xs4[c] = xg[c];
+        for (int c = tid; c < nch; c += nthr) xs4[c] = xg[c];
     } else {
         float* xs = reinterpret_cast<float*>(xs4);
-        for (int i = threadIdx.x; i < H; i += blockDim.x) xs[i] = p.x[i];
+        for (int i = tid; i < H; i += nthr) xs[i] = p.x[i];
     }
-    for (int i = threadIdx.x; i < (p.hd >> 1); i += blockDim.x) freq_s[i] = p.inv_freq[i];
+}
+
+// Shared partial sums of h^2, one per staging warp.
+__device__ __forceinline__ float* norm_partials() {
+    __shared__ float red_s[32];
+    return red_s;
+}
+
+// RMSNorm(h) = (h * w) * inv with inv = 1 / sqrt(sum(h^2) / H + eps) a scalar of the
+// layer, so y = W RMSNorm(h) = inv * (W (h * w)): stage x' = h * w (p.x being h and
+// p.norm_w w) and, in the same pass, each warp's sum of h^2 (each thread its elements
+// in order, then a warp tree); norm_inv() adds the warps in order after the caller's
+// barrier, and the kernel scales each dot product by inv.  The reduction so runs beside
+// the staging instead of in front of it.
+template <typename WT, bool VEC>
+__device__ __forceinline__ void stage_normed(const DecodeParams& p, float4* xs4, int tid, int nthr) {
+    const int H = p.H;
+    const float* nw = p.norm_w;
+    float ss = 0.f;
+    const float4* nw4 = reinterpret_cast<const float4*>(nw);  // 16-byte aligned (checked on the host)
+    auto take4 = [&](float4 h, int i4) {
+        const float4 w = nw4[i4];
+        ss = __fmaf_rn(h.x, h.x, ss);
+        ss = __fmaf_rn(h.y, h.y, ss);
+        ss = __fmaf_rn(h.z, h.z, ss);
+        ss = __fmaf_rn(h.w, h.w, ss);
+        return make_float4(__fmul_rn(h.x, w.x), __fmul_rn(h.y, w.y), __fmul_rn(h.z, w.z), __fmul_rn(h.w, w.w));
+    };
+    if constexpr (VEC && sizeof(WT) == 2) {
+        const int nch = H / 8;
+        const float4* xg = reinterpret_cast<const float4*>(p.x);
+#pragma unroll 4
+        for (int c = tid; c < nch; c += nthr) {
+            xs4[c] = take4(xg[2 * c], 2 * c);
+            xs4[nch + c] = take4(xg[2 * c + 1], 2 * c + 1);
+        }
+    } else if constexpr (VEC) {
+        const int nch = H / 4;
+        const float4* xg = reinterpret_cast<const float4*>(p.x);
+#pragma unroll 4
+        for (int c = tid; c < nch; c += nthr) xs4[c] = take4(xg[c], c);
+    } else {
+        float* xs = reinterpret_cast<float*>(xs4);
+#pragma unroll 4
+        for (int i = tid; i < H; i += nthr) {
+            const float h = p.x[i];
+            ss = __fmaf_rn(h, h, ss);
+            xs[i] = __fmul_rn(h, nw[i]);
+        }
+    }
+    ss = warp_sum(ss);
+    if ((tid & 31) == 0) norm_partials()[tid >> 5] = ss;
+}
+
+// The norm weight is a parameter: its lines can be brought into L1 before the
+// dependency wait, so the staging after it finds them there.
+__device__ __forceinline__ void prefetch_norm(const DecodeParams& p, int tid, int nthr) {
+    if (p.norm_w == nullptr) return;
+    for (int i = tid * 32; i < p.H; i += nthr * 32)
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(p.norm_w + i));
+}
+
+// 1 / sqrt(sum(h^2) / H + eps) from the staging warps' partials (after the barrier that
+// follows the staging), or 1 for a layer without a norm.
+__device__ __forceinline__ float norm_inv(const DecodeParams& p, int nthr) {
+    if (p.norm_w == nullptr) return 1.f;
+    const float* red = norm_partials();
+    float tot = red[0];
+    for (int w = 1; w < nthr / 32; ++w) tot = __fadd_rn(tot, red[w]);
+    return __fdiv_rn(1.f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, static_cast<float>(p.H)), p.norm_eps)));
+}
+
+// The projection input: h * w and the partials of sum(h^2) when the layer has a norm
+// weight (the kernel then scales its dot products by norm_inv), else x as given.
+template <typename WT, bool VEC>
+__device__ __forceinline__ void stage_input(const DecodeParams& p, float4* xs4, int tid, int nthr) {
+    if (p.norm_w != nullptr)
+        stage_normed<WT, VEC>(p, xs4, tid, nthr);
+    else
+        stage_plain<WT, VEC>(p, xs4, tid, nthr);
 }
 
 template <typename WT, bool VEC, int MODE>
@@ -270,9 +352,12 @@ __global__ void __launch_bounds__(256) qkv_decode_kernel(const __grid_constant__
 
     // Inputs written upstream (x, pos) are read, and outputs written, only
     // after the preceding grid in the stream has completed.
+    prefetch_norm(p, threadIdx.x, blockDim.x);
     griddep_wait();
-    stage_x<WT, VEC>(p, smem4, freq_s);
+    stage_input<WT, VEC>(p, smem4, threadIdx.x, blockDim.x);
+    for (int i = threadIdx.x; i < (p.hd >> 1); i += blockDim.x) freq_s[i] = p.inv_freq[i];
     __syncthreads();
+    const float inv = norm_inv(p, blockDim.x);
     const int pos = (MODE == kFused) ? *p.pos : 0;
     const bool store = pos_ok(pos, p.n_ctx);
     griddep_launch_dependents();
@@ -288,6 +373,10 @@ __global__ void __launch_bounds__(256) qkv_decode_kernel(const __grid_constant__
         else dot2_scalar<WT>(w + r0 * H, w + r1 * H, reinterpret_cast<const float*>(smem4), p.H, lane, a0, a1);
         a0 = warp_sum(a0);
         a1 = warp_sum(a1);
+        if (p.norm_w != nullptr) {
+            a0 = __fmul_rn(a0, inv);
+            a1 = __fmul_rn(a1, inv);
+        }
         if (lane == 0) {
             if constexpr (MODE == kProjectOnly) {
                 p.out[sec][r0] = a0;
@@ -520,24 +609,15 @@ __global__ void __launch_bounds__((kGroups * kGroupWarps + 1) * 32, 2)
     }
 
     // ---- consumers ----
+    prefetch_norm(p, threadIdx.x, kConsumerWarps * 32);
     griddep_wait();
     {
-        const int H = p.H;
         const int tid = threadIdx.x, nthr = kConsumerWarps * 32;
-        if constexpr (sizeof(WT) == 2) {
-            const int nch = H / 8;
-            const float4* xg = reinterpret_cast<const float4*>(p.x);
-            for (int c = tid; c < nch; c += nthr) {
-                xs4[c] = xg[2 * c];
-                xs4[nch + c] = xg[2 * c + 1];
-            }
-        } else {
-            const float4* xg = reinterpret_cast<const float4*>(p.x);
-            for (int c = tid; c < H / 4; c += nthr) xs4[c] = xg[c];
-        }
+        stage_input<WT, true>(p, xs4, tid, nthr);
         for (int i = tid; i < half; i += nthr) freq_s[i] = p.inv_freq[i];
     }
     named_barrier_sync(1, kConsumerWarps * 32);
+    const float inv = norm_inv(p, kConsumerWarps * 32);
     const int pos = (MODE == kFused) ? *p.pos : 0;
     const bool store = pos_ok(pos, p.n_ctx);
     if (MODE == kFused && !store && blockIdx.x == 0 && threadIdx.x == 0) flag_bad_pos(pos);
@@ -586,6 +666,10 @@ __global__ void __launch_bounds__((kGroups * kGroupWarps + 1) * 32, 2)
             }
             if (last && gw == 0 && lane == 0) mbar_arrive(&empty[s]);
             if (gw == 0 && lane == 0) {
+                if (p.norm_w != nullptr) {
+                    a0 = __fmul_rn(a0, inv);
+                    a1 = __fmul_rn(a1, inv);
+                }
                 if constexpr (MODE == kProjectOnly) {
                     p.out[t.sec][r0] = a0;
                     p.out[t.sec][r1] = a1;
@@ -724,24 +808,16 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
             bias_s[e] = j < t.n ? __ldg(p.bias[t.sec] + (blk ? t.r + t.off : t.r) + j) : 0.f;
         }
     }
+    prefetch_norm(p, threadIdx.x, kGroups * 32);
     griddep_wait();
     {
-        constexpr bool kBf16 = sizeof(WT) == 2;
-        const int nch = p.H / (kBf16 ? 8 : 4);
         const int tid = threadIdx.x, nthr = kGroups * 32;
-        const float4* xg = reinterpret_cast<const float4*>(p.x);
-        if constexpr (kBf16) {
-            for (int c = tid; c < nch; c += nthr) {
-                xs4[c] = xg[2 * c];
-                xs4[nch + c] = xg[2 * c + 1];
-            }
-        } else {
-            for (int c = tid; c < nch; c += nthr) xs4[c] = xg[c];
-        }
+        stage_input<WT, true>(p, xs4, tid, nthr);
         if (EPI == kEpiQkv)
             for (int i = tid; i < (p.hd >> 1); i += nthr) freq_s[i] = p.inv_freq[i];
     }
     named_barrier_sync(1, kGroups * 32);
+    const float inv = norm_inv(p, kGroups * 32);
     const int pos = (MODE == kFused && EPI == kEpiQkv) ? *p.pos : 0;
     const bool store = pos_ok(pos, p.n_ctx);
     if (MODE == kFused && EPI == kEpiQkv && !store && blockIdx.x == 0 && threadIdx.x == 0) flag_bad_pos(pos);
@@ -765,6 +841,10 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
             if (j < t.n) dot2_staged<WT>(sp + j * row_bytes, sp + j1 * row_bytes, xs4, p.H, lane, a0, a1);
             y[j] = a0;
             if (j + 1 < kBlkPairs) y[j + 1] = a1;
+        }
+        if (p.norm_w != nullptr) {
+#pragma unroll
+            for (int j = 0; j < kBlkPairs; ++j) y[j] = __fmul_rn(y[j], inv);
         }
         __syncwarp();  // every lane is done reading the stage
         if (lane == 0) mbar_arrive(&empty[st]);

@@ -83,10 +83,14 @@ int use_vec(const qkv_plan* plan, const float* x, const void* const w[3]) {
     return plan->vec && aligned16(x) && aligned16(w[0]) && aligned16(w[1]) && aligned16(w[2]);
 }
 
+// `norm_w` non-null: x is the hidden state h and the kernel projects RMSNorm(h).
 qkv_status run_decode(const qkv_plan* plan, const float* x, const void* const w[3],
                       const float* const b[3], const int32_t* d_pos, float* q, float* k, float* v,
-                      void* kv_k, void* kv_v, bool pdl, cudaStream_t s) {
+                      void* kv_k, void* kv_v, bool pdl, cudaStream_t s, const float* norm_w = nullptr,
+                      float norm_eps = 0.f) {
     DecodeParams p = base_params(plan);
+    p.norm_w = norm_w;
+    p.norm_eps = norm_eps;
     p.x = x;
     for (int i = 0; i < 3; ++i) {
         p.w[i] = w[i];
@@ -218,6 +222,27 @@ extern "C" qkv_status qkv_decode_step(const qkv_plan* plan, const float* x, cons
     if (st != QKV_OK) return st;
     return run_decode(plan, x, ws, bs, d_pos, q, k, v, kv_k, kv_v, false,
                       static_cast<cudaStream_t>(stream));
+}
+
+extern "C" qkv_status qkv_decode_step_rmsnorm(const qkv_plan* plan, const float* h, const float* norm_w,
+                                              float norm_eps, const void* w, const float* bias,
+                                              const int32_t* d_pos, float* q, float* k, float* v, void* kv_k,
+                                              void* kv_v, void* stream) {
+    REQUIRE(plan, "plan is null");
+    REQUIRE(plan->d.layer_class == QKV_CLASS_CONCAT, "qkv_decode_step_rmsnorm needs a concat-class plan");
+    REQUIRE(norm_w, "norm_w is null");
+    REQUIRE(aligned16(norm_w), "norm_w must be 16-byte aligned");
+    REQUIRE(norm_eps >= 0.f && norm_eps == norm_eps, "norm_eps must be a number >= 0");
+    REQUIRE(w && bias, "w or bias is null");
+    const size_t es = elem_size(plan->d.w_dtype);
+    const char* wb = static_cast<const char*>(w);
+    const void* ws[3] = {wb, wb + plan->nqt * plan->d.hidden * es,
+                         wb + (plan->nqt + plan->nkt) * plan->d.hidden * es};
+    const float* bs[3] = {bias, bias + plan->nqt, bias + plan->nqt + plan->nkt};
+    qkv_status st = check_decode_ptrs(plan, h, ws, bs, d_pos, q, k, v, kv_k, kv_v);
+    if (st != QKV_OK) return st;
+    return run_decode(plan, h, ws, bs, d_pos, q, k, v, kv_k, kv_v, false, static_cast<cudaStream_t>(stream),
+                      norm_w, norm_eps);
 }
 
 extern "C" qkv_status qkv_decode_step_mixed(const qkv_plan* plan, const float* x, const void* wq,
@@ -429,9 +454,37 @@ namespace {
 qkv_status finish_capture(cudaStream_t s, qkv_status st, qkv_graph** out);
 }
 
+namespace {
+qkv_status model_graph_create(const qkv_plan* const* plans, int32_t n_layers, const qkv_layer_ptrs* layers,
+                              const float* const* norm_w, float norm_eps, const int32_t* d_pos, void* stream,
+                              qkv_graph** out);
+}
+
 extern "C" qkv_status qkv_model_graph_create(const qkv_plan* const* plans, int32_t n_layers,
                                              const qkv_layer_ptrs* layers, const int32_t* d_pos,
                                              void* stream, qkv_graph** out) {
+    return model_graph_create(plans, n_layers, layers, nullptr, 0.f, d_pos, stream, out);
+}
+
+extern "C" qkv_status qkv_model_graph_create_rmsnorm(const qkv_plan* const* plans, int32_t n_layers,
+                                                     const qkv_layer_ptrs* layers, const float* const* norm_w,
+                                                     float norm_eps, const int32_t* d_pos, void* stream,
+                                                     qkv_graph** out) {
+    REQUIRE(out, "out is null");
+    *out = nullptr;
+    REQUIRE(norm_w, "norm_w is null");
+    REQUIRE(norm_eps >= 0.f && norm_eps == norm_eps, "norm_eps must be a number >= 0");
+    for (int32_t i = 0; i < n_layers; ++i) {
+        REQUIRE(norm_w[i], "norm weight of layer %d is null", i);
+        REQUIRE(aligned16(norm_w[i]), "norm weight of layer %d must be 16-byte aligned", i);
+    }
+    return model_graph_create(plans, n_layers, layers, norm_w, norm_eps, d_pos, stream, out);
+}
+
+namespace {
+qkv_status model_graph_create(const qkv_plan* const* plans, int32_t n_layers, const qkv_layer_ptrs* layers,
+                              const float* const* norm_w, float norm_eps, const int32_t* d_pos, void* stream,
+                              qkv_graph** out) {
     REQUIRE(out, "out is null");
     *out = nullptr;
     REQUIRE(plans && layers && d_pos, "null argument");
@@ -476,10 +529,12 @@ extern "C" qkv_status qkv_model_graph_create(const qkv_plan* const* plans, int32
             bs[1] = L.bias_k;
             bs[2] = L.bias_v;
         }
-        st = run_decode(p, L.x, ws, bs, d_pos, L.q, L.k, L.v, L.kv_k, L.kv_v, i > 0, s);
+        st = run_decode(p, L.x, ws, bs, d_pos, L.q, L.k, L.v, L.kv_k, L.kv_v, i > 0, s,
+                        norm_w ? norm_w[i] : nullptr, norm_eps);
     }
     return finish_capture(s, st, out);
 }
+}  // namespace
 
 namespace {
 

@@ -26,6 +26,8 @@ struct DecodeParams {
     const int32_t* pos;     // device position
     int32_t H, nqt, nkt, hd, n_ctx, kv_f16;
     int32_t nf;             // FusedFFN: rows per half of the gate|up weight (0 for the QKV stage)
+    const float* norm_w;    // RMSNorm weight [H]: x is then the hidden state h, normalised in-kernel
+    float norm_eps;         // RMSNorm epsilon
     float inv_freq[QKV_MAX_HEAD_DIM / 2];
 };
 

@@ -174,3 +174,23 @@ def test_ffn_guards(lib):
     assert g(64, 8, q.QKV_BF16, 1, layers, None, ctypes.byref(h)) == q.QKV_ERR_INVALID_ARG
     assert g(64, 8, q.QKV_BF16, 1, layers, 16, ctypes.byref(h)) == q.QKV_ERR_INVALID_ARG  # null layer 0
 
+
+def test_rmsnorm_guards(lib):
+    """The fused RMSNorm entry points validate the norm arguments on the host."""
+    p = q.qkv_plan_create(64, 2, 1, 8, 1e4, 16)
+    for args in ((None, 1e-6), (16, -1.0), (16, float("nan"))):
+        with pytest.raises(q.QkvError) as e:
+            q.qkv_decode_step_rmsnorm(p, 16, args[0], args[1], 16, 16, 16, 16, 16, 16, 16, 16, stream=0)
+        assert e.value.status == q.QKV_ERR_INVALID_ARG
+    mixed = q.qkv_plan_create(64, 2, 1, 8, 1e4, 16, layer_class=q.QKV_CLASS_MIXED)
+    with pytest.raises(q.QkvError) as e:
+        q.qkv_decode_step_rmsnorm(mixed, 16, 16, 1e-6, 16, 16, 16, 16, 16, 16, 16, 16, stream=0)
+    assert e.value.status == q.QKV_ERR_INVALID_ARG
+    h = ctypes.c_void_p()
+    plans = (ctypes.c_void_p * 1)(p.handle)
+    layers = (q.qkv_layer_ptrs * 1)()
+    norms = (ctypes.c_void_p * 1)(None)
+    g = lib.qkv_model_graph_create_rmsnorm
+    assert g(plans, 1, layers, None, ctypes.c_float(1e-6), 16, 16, ctypes.byref(h)) == q.QKV_ERR_INVALID_ARG
+    assert g(plans, 1, layers, norms, ctypes.c_float(1e-6), 16, 16, ctypes.byref(h)) == q.QKV_ERR_INVALID_ARG
+
