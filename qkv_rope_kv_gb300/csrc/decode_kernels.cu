@@ -488,6 +488,17 @@ __host__ __device__ __forceinline__ int unit_count(int nqt, int nkt, int hd) {
     return (nqt / hd) * per_head + (nkt / hd) * per_head + (nkt + 2 * P - 1) / (2 * P);
 }
 
+// First unit of CTA b of `grid` when `units` are split in contiguous ranges:
+// units * F(b / grid) with F(x) = x + (skew / 100) x (1 - x).  CTAs of a chained
+// launch are dispatched in block order as the previous grid's SMs free up, so later
+// blocks start later; skew > 0 gives them proportionally less (the first block
+// 1 + skew/100 times the mean share, the last 1 - skew/100) and the ranges end
+// together.  skew = 0 is the even split.  Monotone for 0 <= skew <= 100.
+__host__ __device__ __forceinline__ int unit_split(int units, int b, int grid, int skew) {
+    const long long u = units, bb = b, g = grid;
+    return static_cast<int>((u * bb * (100 * g + skew * (g - bb))) / (100 * g * g));
+}
+
 __device__ __forceinline__ uint4 ld_shared_v4(const void* p) {
     uint4 r;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -550,7 +561,7 @@ __device__ __forceinline__ void dot2_staged(const unsigned char* row0, const uns
 template <typename WT, int MODE, int kGroups>
 __global__ void __launch_bounds__((kGroups * kGroupWarps + 1) * 32, 2)
     qkv_decode_tma_kernel(const __grid_constant__ DecodeParams p, int stages, uint32_t stage_bytes,
-                          uint32_t x_bytes) {
+                          uint32_t x_bytes, int skew) {
     constexpr int kConsumerWarps = kGroups * kGroupWarps;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float freq_s[QKV_MAX_HEAD_DIM / 2];
@@ -563,8 +574,8 @@ __global__ void __launch_bounds__((kGroups * kGroupWarps + 1) * 32, 2)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int half = p.hd >> 1;
     const int units = unit_count(p.nqt, p.nkt, p.hd);
-    const int u_begin = static_cast<int>(static_cast<long long>(units) * blockIdx.x / gridDim.x);
-    const int u_end = static_cast<int>(static_cast<long long>(units) * (blockIdx.x + 1) / gridDim.x);
+    const int u_begin = unit_split(units, blockIdx.x, gridDim.x, skew);
+    const int u_end = unit_split(units, blockIdx.x + 1, gridDim.x, skew);
     const int n = u_end - u_begin;
     const uint32_t row_bytes = static_cast<uint32_t>(p.H) * sizeof(WT);
 
@@ -736,7 +747,7 @@ __device__ __forceinline__ float swiglu(float g, float u) {
 template <typename WT, int MODE, int kGroups, int EPI>
 __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
     qkv_decode_blk_kernel(const __grid_constant__ DecodeParams p, int stages, uint32_t stage_bytes,
-                          uint32_t x_bytes, int max_units) {
+                          uint32_t x_bytes, int max_units, int skew) {
     static_assert(kBlkPairs >= 1 && kBlkPairs <= 8, "rows per block");
     static_assert(kGroupWarps == 1, "one warp per consumer group");
     extern __shared__ __align__(128) unsigned char smem[];
@@ -751,8 +762,8 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int units = blk_unit_count<EPI>(p);
-    const int u_begin = static_cast<int>(static_cast<long long>(units) * blockIdx.x / gridDim.x);
-    const int u_end = static_cast<int>(static_cast<long long>(units) * (blockIdx.x + 1) / gridDim.x);
+    const int u_begin = unit_split(units, blockIdx.x, gridDim.x, skew);
+    const int u_end = unit_split(units, blockIdx.x + 1, gridDim.x, skew);
     const int n = 2 * (u_end - u_begin);
     const uint32_t row_bytes = static_cast<uint32_t>(p.H) * sizeof(WT);
 
@@ -990,6 +1001,17 @@ int sm_count() {
 #define QKV_DECODE_MAX_STAGES 32
 #endif
 constexpr int kMaxStages = QKV_DECODE_MAX_STAGES;
+// Work skew (percent) of the ring kernels in a chained launch: see unit_split.  The
+// pair ring (rows < 8 KB: 7B-size layers, 8 us each) gains from it (+4 % at 20 on the 7B
+// graph); the block ring's 12-unit shares are too coarse to skew without imbalance.
+#ifndef QKV_DECODE_CHAIN_SKEW_PAIR
+#define QKV_DECODE_CHAIN_SKEW_PAIR 20
+#endif
+#ifndef QKV_DECODE_CHAIN_SKEW_BLOCK
+#define QKV_DECODE_CHAIN_SKEW_BLOCK 0
+#endif
+constexpr int kChainSkewPair = QKV_DECODE_CHAIN_SKEW_PAIR;
+constexpr int kChainSkewBlock = QKV_DECODE_CHAIN_SKEW_BLOCK;
 
 struct RingShape {
     int stages;        // multiple of the group count
@@ -1037,7 +1059,9 @@ cudaError_t launch_decode_tma(const DecodeParams& p, const RingShape& r, bool pd
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kernel, p, r.stages, r.stage_bytes, r.x_bytes);
+    // a skew needs a few units per CTA to move; below that it only unbalances
+    const int skew = (pdl && units >= 4 * grid) ? kChainSkewPair : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, p, r.stages, r.stage_bytes, r.x_bytes, skew);
 }
 
 
@@ -1052,7 +1076,12 @@ cudaError_t launch_decode_blk(const DecodeParams& p, int ctas_per_sm, int smem_k
     const int units = EPI == kEpiQkv ? unit_count<kBlkPairs>(p.nqt, p.nkt, p.hd) : (p.nf + kBlkPairs - 1) / kBlkPairs;
     const int ctas_max = sm_count() * ctas_per_sm;
     const int grid = units < ctas_max ? units : ctas_max;
-    const int max_units = (units + grid - 1) / grid;
+    const int skew = pdl ? kChainSkewBlock : 0;
+    int max_units = 0;
+    for (int b = 0; b < grid; ++b) {
+        const int nb = unit_split(units, b + 1, grid, skew) - unit_split(units, b, grid, skew);
+        max_units = nb > max_units ? nb : max_units;
+    }
     // per unit: staged biases, published results and a counter
     const size_t tail = static_cast<size_t>(max_units) * (4 * kBlkPairs * sizeof(float) + sizeof(int));
     const size_t budget = static_cast<size_t>(smem_kb) * 1024;
@@ -1077,7 +1106,7 @@ cudaError_t launch_decode_blk(const DecodeParams& p, int ctas_per_sm, int smem_k
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     launched = true;
-    return cudaLaunchKernelEx(&cfg, kernel, p, stages, stage_bytes, x_bytes, max_units);
+    return cudaLaunchKernelEx(&cfg, kernel, p, stages, stage_bytes, x_bytes, max_units, skew);
 }
 
 template <typename WT, bool VEC, int MODE>
