@@ -37,8 +37,7 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 126 * 1024 * 1024
 METRIC = "decode QKV layers/sec and achieved HBM GB/s (fraction of GB300 peak), 1 GPU"
-DECODE_KERNEL_SRC = os.path.join(ROOT, "qkv_rope_kv_gb300", "csrc", "decode_kernels.cu")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
 
 def parse():
@@ -72,22 +71,22 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def decode_source_hash() -> str:
-    with open(DECODE_KERNEL_SRC, "rb") as fh:
+def source_hash(rel_path: str) -> str:
+    with open(os.path.join(ROOT, rel_path), "rb") as fh:
         return hashlib.sha256(fh.read()).hexdigest()
 
 
 def traffic_per_launch(workload_name: str):
-    """DRAM bytes per projection launch from a committed ncu capture, if the kernel source
-    is unchanged since the capture; else None."""
+    """(DRAM bytes per launch, kernel) of the workload's dominant kernel from a committed ncu
+    capture, if that kernel's source file is unchanged since the capture; else (None, None)."""
     try:
         with open(TRAFFIC_FILE) as fh:
-            t = json.load(fh)
+            t = json.load(fh)["captures"][workload_name]
+        if t["source_sha256"] != source_hash(t["source"]):
+            return None, None
+        return int(t["bytes_per_launch"]), t["kernel"]
     except Exception:
-        return None
-    if t.get("source_sha256") != decode_source_hash():
-        return None
-    return t.get("bytes_per_launch", {}).get(workload_name)
+        return None, None
 
 
 # ---------------------------------------------------------------- clocks
@@ -481,7 +480,7 @@ def native_arm(args, w):
     algo = w.algo_bytes_per_layer()
     achieved = algo / per_layer_s / 1e9
     peak, peak_kind = measured_peak()
-    traffic = traffic_per_launch(w.name)
+    traffic, traffic_kernel = traffic_per_launch(w.name)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -500,7 +499,8 @@ def native_arm(args, w):
                          "frac": achieved / peak, "peak_kind": peak_kind,
                          "frac_of_nominal_8000": achieved / NOMINAL_HBM_GBS,
                          "traffic": traffic, "algo_bytes_per_launch": algo,
-                         "kernel": "qkv_decode_kernel (fused projection + bias/RoPE/KV-store tail)",
+                         "kernel": traffic_kernel or "qkv_decode ring kernel (fused projection + "
+                                                     "bias/RoPE/KV-store tail)",
                          "duration_basis": "step time / %d launches (back-to-back graph replay)" % w.n_layers},
             "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": kernels * args.steps,
             "launches_per_step": kernels, "clocks": clk,
@@ -579,7 +579,8 @@ def prefill_arm(args, w):
             "roofline": {"bound": "hbm", "achieved": algo_b / per_layer / 1e9, "peak": peak, "unit": "GB/s",
                          "frac": algo_b / per_layer / 1e9 / peak, "peak_kind": peak_kind,
                          "frac_of_nominal_8000": algo_b / per_layer / 1e9 / NOMINAL_HBM_GBS,
-                         "traffic": None, "algo_bytes_per_launch": algo_b, "algo_flops_per_launch": algo_f,
+                         "traffic": traffic_per_launch(w.name)[0], "algo_bytes_per_launch": algo_b,
+                         "algo_flops_per_launch": algo_f,
                          "kernel": "qkv_prefill_kernel (tcgen05 bf16 GEMM + bias/RoPE/KV-store epilogue)",
                          "duration_basis": "step time / %d launches" % w.n_layers},
             "gpu_launches": graph.kernel_count * args.steps, "launches_per_step": graph.kernel_count,
@@ -681,7 +682,7 @@ def ffn_arm(args, w):
             "roofline": {"bound": "hbm", "achieved": algo / per_layer / 1e9, "peak": peak, "unit": "GB/s",
                          "frac": algo / per_layer / 1e9 / peak, "peak_kind": peak_kind,
                          "frac_of_nominal_8000": algo / per_layer / 1e9 / NOMINAL_HBM_GBS,
-                         "traffic": None, "algo_bytes_per_launch": algo,
+                         "traffic": traffic_per_launch(w.name)[0], "algo_bytes_per_launch": algo,
                          "kernel": "qkv_decode_blk_kernel (gate|up GEMV + SwiGLU tail)",
                          "duration_basis": "step time / %d launches (back-to-back graph replay)" % L},
             "e2e": e2e, "cpu_baseline": cpu,

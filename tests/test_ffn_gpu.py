@@ -2,12 +2,13 @@
 concat gate|up weight (page "06 · Assign + fusion — every node picks an engine, then
 patterns fold", §2.2-2.3), element by element at the FFN shapes of Qwen2.5-0.5B (f32),
 7B and 14B (bf16) and at small ragged ones; the PDL-chained graph against sequential
-steps, bitwise."""
+steps, bitwise; and the whole-model graphs the FFN workloads time (24, 28 and 48
+layers), every layer against the oracle."""
 import numpy as np
 import pytest
 
 from gpu_helpers import assert_f32_close, to_dev, to_host
-from qkv_rope_kv_gb300 import synth
+from qkv_rope_kv_gb300 import configs, synth
 
 pytestmark = pytest.mark.gpu
 
@@ -79,3 +80,41 @@ def test_ffn_graph_equals_steps_bitwise(qkv):
     for og, (_, _, os_) in zip(outs_graph, outs_step):
         a, b = to_host(og), to_host(os_)
         assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+@pytest.mark.parametrize("w", [configs.QWEN05_FFN, configs.QWEN7B_FFN, configs.QWEN14B_FFN], ids=lambda w: w.name)
+def test_ffn_model_graph_full_size(orc, qkv, w):
+    """The L-layer graph with the bench's inputs (seed 0, x of layer l = hidden(100 + l)):
+    every layer's output against the oracle, and the first and last layers against a
+    direct qkv_ffn_step, bitwise."""
+    import torch
+    L = w.n_layers
+    dt = qkv.QKV_BF16 if w.w_dtype == "bf16" else qkv.QKV_F32
+    dx = torch.empty(L, w.hidden, dtype=torch.float32, device="cuda")
+    dout = torch.full((L, w.n_ff), float("nan"), dtype=torch.float32, device="cuda")
+    hostW = np.empty((2 * w.n_ff, w.hidden), np.uint16 if w.w_dtype == "bf16" else np.float32)
+    layers, keep, want = [], [], []
+    for l in range(L):
+        synth.ffn_weight_rows(SEED, l, 0, 2 * w.n_ff, w.hidden, w.w_dtype, out=hostW)
+        x = synth.hidden(SEED, 100 + l, 0, w.hidden)
+        want.append(orc.ffn_swiglu(hostW, x))
+        dW = to_dev(hostW)
+        dx[l].copy_(to_dev(x))
+        keep.append(dW)
+        layers.append(dict(x=dx[l], w_gate_up=dW, out=dout[l]))
+    stream = torch.cuda.Stream()
+    g = qkv.qkv_ffn_graph_create(w.hidden, w.n_ff, dt, layers, stream)
+    assert g.kernel_count == L
+    torch.cuda.synchronize()
+    g.launch(stream)
+    stream.synchronize()
+    flags, _ = qkv.qkv_check_device_error(stream)
+    assert flags == 0
+    got = to_host(dout)
+    for l in range(L):
+        assert_f32_close(got[l], want[l], "%s layer %d" % (w.name, l))
+    for l in (0, L - 1):
+        o = torch.full((w.n_ff,), float("nan"), dtype=torch.float32, device="cuda")
+        qkv.qkv_ffn_step(w.hidden, w.n_ff, dt, dx[l], keep[l], o, stream=stream.cuda_stream)
+        stream.synchronize()
+        assert np.array_equal(to_host(o).view(np.uint32), got[l].view(np.uint32))
