@@ -69,6 +69,11 @@ def _bind(lib):
     lib.oracle_silu.restype = d
     lib.oracle_ffn_swiglu.argtypes = [vp, i, vp, i64, i64, vp]
     lib.oracle_rmsnorm.argtypes = [vp, vp, i64, d, vp]
+    lib.oracle_qkv_token_qknorm.argtypes = [vp, vp, vp, vp, d, i, i, i, d, d, i, i, i, vp, vp, vp, vp, vp]
+    lib.oracle_qkv_token_qknorm.restype = i
+    lib.oracle_qkv_decode_qknorm.argtypes = [vp, i, vp, vp, vp, vp, d, i, i, i, i, d, d, i, i, i, vp, vp, vp,
+                                             vp, vp, vp]
+    lib.oracle_qkv_decode_qknorm.restype = i
     return lib
 
 
@@ -158,6 +163,43 @@ class Oracle:
                                        _p(np.ascontiguousarray(bias, np.float32)), nh, nkv, hd,
                                        base, freq_scale, pos, n_ctx, f16, _p(q), _p(k), _p(v),
                                        _p(kv_k), _p(kv_v))
+        return st, q, k, v
+
+    def token_qknorm(self, y, bias, q_norm_w, k_norm_w, eps, nh, nkv, hd, base, freq_scale, pos, kv_k, kv_v):
+        """FusedQkvNorm epilogue for one token on a precomputed projection y (float64 [R])."""
+        nqt, nkt = nh * hd, nkv * hd
+        q = np.empty(nqt, np.float32)
+        k = np.empty(nkt, np.float32)
+        v = np.empty(nkt, np.float32)
+        n_ctx, f16 = _kv_meta(kv_k, kv_v, nkt)
+        st = self.lib.oracle_qkv_token_qknorm(_p(np.ascontiguousarray(y, np.float64)),
+                                              _p(np.ascontiguousarray(bias, np.float32)),
+                                              _p(np.ascontiguousarray(q_norm_w, np.float32)),
+                                              _p(np.ascontiguousarray(k_norm_w, np.float32)), float(eps), nh, nkv,
+                                              hd, base, freq_scale, pos, n_ctx, f16, _p(q), _p(k), _p(v),
+                                              _p(kv_k), _p(kv_v))
+        return st, q, k, v
+
+    def decode_qknorm(self, W, x, bias, q_norm_w, k_norm_w, eps, nh, nkv, hd, base, freq_scale, pos, kv_k, kv_v):
+        """Concat-class FusedQkvNorm: projection, bias, per-head q/k RMSNorm (weights of hd values),
+        neox RoPE, KV store.  kv_k/kv_v updated in place as in decode()."""
+        nqt, nkt = nh * hd, nkv * hd
+        R = nqt + 2 * nkt
+        W = np.ascontiguousarray(W)
+        assert W.shape[0] == R
+        assert len(q_norm_w) == hd and len(k_norm_w) == hd
+        y = np.empty(R, np.float64)
+        q = np.empty(nqt, np.float32)
+        k = np.empty(nkt, np.float32)
+        v = np.empty(nkt, np.float32)
+        n_ctx, f16 = _kv_meta(kv_k, kv_v, nkt)
+        st = self.lib.oracle_qkv_decode_qknorm(_p(W), int(W.dtype == np.uint16),
+                                               _p(np.ascontiguousarray(x, np.float32)),
+                                               _p(np.ascontiguousarray(bias, np.float32)),
+                                               _p(np.ascontiguousarray(q_norm_w, np.float32)),
+                                               _p(np.ascontiguousarray(k_norm_w, np.float32)), float(eps),
+                                               W.shape[1], nh, nkv, hd, base, freq_scale, pos, n_ctx, f16, _p(y),
+                                               _p(q), _p(k), _p(v), _p(kv_k), _p(kv_v))
         return st, q, k, v
 
     def decode(self, W, x, bias, nh, nkv, hd, base, freq_scale, pos, kv_k, kv_v):

@@ -25,6 +25,14 @@
  *     name it without its formula, so the oracle takes the plain definition
  *     x_c = h_c * w_c / sqrt(mean(h^2) + eps)).
  *
+ *   - "06 · Assign + fusion ...", §3 (the backend capability tables: FusedQkvNorm,
+ *     the Qwen3 per-head-norm variant of FusedQKV, whose epilogue normalises each
+ *     q and k head before the same bias / rope / store).  The pages give no
+ *     formula; the oracle takes the plain reading: after the bias, each head of q
+ *     (and of k) is replaced by z * w / sqrt(mean over the head's hd values of
+ *     z^2 + eps), w a weight of hd values shared by the heads of q (another for
+ *     k), then rotated and stored as before; v is not normalised.
+ *
  * Precision: everything is carried in double; results are rounded to f32 (or
  * f32 then f16) only where the stage stores them.  Readings taken where the
  * pages are open:
@@ -287,4 +295,64 @@ void oracle_rmsnorm(const float* h, const float* w, int64_t H, double eps, float
     for (int64_t c = 0; c < H; ++c) ss += (double)h[c] * (double)h[c];
     const double inv = 1.0 / sqrt(ss / (double)H + eps);
     for (int64_t c = 0; c < H; ++c) x[c] = (float)((double)h[c] * inv * (double)w[c]);
+}
+
+/* ---- FusedQkvNorm: per-head RMSNorm of q and k before the rotation -------- */
+
+/* One head of width hd: z_i = y_i + b_i, inv = 1 / sqrt( (1/hd) sum_i z_i^2 + eps ),
+ * n_i = z_i * inv * w_i, then the neox pairs (n_d, n_{d+hd/2}) rotated at `pos`.
+ * Writes the rotated head (f32) to out[0 .. hd-1]. */
+static void qknorm_head(const double* y, const float* b, const float* w, double eps, int hd, double base,
+                        double freq_scale, int pos, float* out) {
+    const int half = hd / 2;
+    double ss = 0.0;
+    for (int i = 0; i < hd; ++i) {
+        const double z = y[i] + (double)b[i];
+        ss += z * z;
+    }
+    const double inv = 1.0 / sqrt(ss / (double)hd + eps);
+    for (int d = 0; d < half; ++d) {
+        const double n0 = (y[d] + (double)b[d]) * inv * (double)w[d];
+        const double n1 = (y[d + half] + (double)b[d + half]) * inv * (double)w[d + half];
+        const float f = oracle_inv_freq(d, hd, base, freq_scale);
+        oracle_rope_pair(n0, n1, 0.0f, 0.0f, pos, f, &out[d], &out[d + half]);
+    }
+}
+
+/* One token of the FusedQkvNorm stage on the projection y = [q | k | v] (double)
+ * with the concatenated bias, q_norm_w[hd] and k_norm_w[hd]: every q head and every
+ * k head through qknorm_head, v biased; k and v stored at row `pos` as in
+ * oracle_qkv_token (same status and range rule). */
+int oracle_qkv_token_qknorm(const double* y, const float* bias, const float* q_norm_w, const float* k_norm_w,
+                            double eps, int nh, int nkv, int hd, double base, double freq_scale, int pos,
+                            int n_ctx, int kv_is_f16, float* q_out, float* k_out, float* v_out, void* kv_k,
+                            void* kv_v) {
+    if (hd <= 0 || (hd % 2) != 0 || nh <= 0 || nkv <= 0 || n_ctx <= 0 || !(eps >= 0.0)) return ORACLE_BAD_ARG;
+    const int nqt = nh * hd, nkt = nkv * hd;
+    const int store = (pos >= 0 && pos < n_ctx);
+    const size_t row = store ? (size_t)pos * (size_t)nkt : 0;
+    for (int h = 0; h < nh; ++h)
+        qknorm_head(y + h * hd, bias + h * hd, q_norm_w, eps, hd, base, freq_scale, pos, q_out + h * hd);
+    for (int h = 0; h < nkv; ++h) {
+        qknorm_head(y + nqt + h * hd, bias + nqt + h * hd, k_norm_w, eps, hd, base, freq_scale, pos,
+                    k_out + h * hd);
+        if (store)
+            for (int i = 0; i < hd; ++i) kv_put(kv_k, kv_is_f16, row + (size_t)(h * hd + i), k_out[h * hd + i]);
+    }
+    for (int j = 0; j < nkt; ++j) {
+        v_out[j] = (float)(y[nqt + nkt + j] + (double)bias[nqt + nkt + j]);
+        if (store) kv_put(kv_v, kv_is_f16, row + (size_t)j, v_out[j]);
+    }
+    return store ? ORACLE_OK : ORACLE_POS_RANGE;
+}
+
+/* Concat class: one [R x H] matrix, then oracle_qkv_token_qknorm. */
+int oracle_qkv_decode_qknorm(const void* W, int w_is_bf16, const float* x, const float* bias,
+                             const float* q_norm_w, const float* k_norm_w, double eps, int hidden, int nh, int nkv,
+                             int hd, double base, double freq_scale, int pos, int n_ctx, int kv_is_f16,
+                             double* y_scratch, float* q_out, float* k_out, float* v_out, void* kv_k, void* kv_v) {
+    const int64_t R = (int64_t)(nh + 2 * nkv) * hd;
+    oracle_matvec(W, w_is_bf16, x, R, hidden, y_scratch);
+    return oracle_qkv_token_qknorm(y_scratch, bias, q_norm_w, k_norm_w, eps, nh, nkv, hd, base, freq_scale, pos,
+                                   n_ctx, kv_is_f16, q_out, k_out, v_out, kv_k, kv_v);
 }

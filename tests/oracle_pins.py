@@ -499,4 +499,87 @@ def pin_rmsnorm_scale_and_weight(orc):
     assert abs(float(np.sqrt(np.sum(base.astype(np.float64) ** 2))) - 8.0) <= 1e-5
 
 
+def _qkn(orc, yq, yk, yv, bias, wq, wk, eps, pos, hd, n_ctx=4, base=1.0e4):
+    """token_qknorm on hand-made sections (f32 cache of n_ctx rows)."""
+    nh, nkv = len(yq) // hd, len(yk) // hd
+    y = np.concatenate([yq, yk, yv]).astype(np.float64)
+    kk = np.zeros((n_ctx, nkv * hd), np.float32)
+    vv = np.zeros((n_ctx, nkv * hd), np.float32)
+    st, q, k, v = orc.token_qknorm(y, np.asarray(bias, np.float32), np.asarray(wq, np.float32),
+                                   np.asarray(wk, np.float32), eps, nh, nkv, hd, base, 1.0, pos, kk, vv)
+    return st, q, k, v, kk, vv
+
+
+def pin_qknorm_closed_forms(orc):
+    """FusedQkvNorm with hd = 2 at pos 0 (no rotation): a head z = (1, 1) has RMS 1, so q = w
+    exactly; z = (0.5, 0.5) gives k = w_k; the bias is added before the norm (y = 0 with
+    bias (2, 2) still normalises to w); eps = 3 on z = (1, 1) gives 1 / sqrt(1 + 3) = 0.5;
+    two q heads are normalised separately; v is y + b, untouched by the norm."""
+    wq, wk = [1.0, 2.0], [3.0, 0.25]
+    st, q, k, v, kk, vv = _qkn(orc, [1, 1], [0.5, 0.5], [3, 4], [0, 0, 0, 0, 0.5, -1], wq, wk, 0.0, 0, 2)
+    assert st == 0
+    assert np.array_equal(q, np.float32(wq)) and np.array_equal(k, np.float32(wk))
+    assert np.array_equal(v, np.float32([3.5, 3.0]))
+    assert np.array_equal(kk[0], k) and np.array_equal(vv[0], v) and not kk[1:].any()
+    st, q, k, v, _, _ = _qkn(orc, [0, 0], [0, 0], [0, 0], [2, 2, -4, -4, 0, 0], wq, wk, 0.0, 0, 2)
+    assert np.array_equal(q, np.float32(wq)) and np.array_equal(k, -np.float32(wk))
+    st, q, k, v, _, _ = _qkn(orc, [1, 1], [1, 1], [0, 0], np.zeros(6), wq, wk, 3.0, 0, 2)
+    assert np.array_equal(q, np.float32([0.5, 1.0])) and np.array_equal(k, np.float32([1.5, 0.125]))
+    # head 0 = (3, 4) (RMS sqrt(12.5)), head 1 = (1, 1): head 1 is w whatever head 0 holds
+    st, q, k, v, _, _ = _qkn(orc, [3, 4, 1, 1], [1, 1], [0, 0], np.zeros(8), wq, wk, 0.0, 0, 2)
+    assert np.array_equal(q[2:], np.float32(wq))
+    want0 = np.float32(np.array([3.0, 8.0]) / np.sqrt(12.5))
+    assert np.all(np.abs(f32_bits(q[:2]).astype(np.int64) - f32_bits(want0).astype(np.int64)) <= 1)
+
+
+def pin_qknorm_norm_before_rotation(orc):
+    """The norm and its weight act before the rotation: z = (1, 1), w = (1, 2), eps = 0 at
+    pos 7 gives n = (1, 2) rotated by theta, i.e. (cos - 2 sin, sin + 2 cos), not the
+    weighted rotation of (1, 1)."""
+    hd, pos, base = 2, 7, 1.0e4
+    th = float(orc.theta(pos, orc.inv_freq(0, hd, base)))
+    c, s_ = np.cos(th), np.sin(th)
+    st, q, _, _, _, _ = _qkn(orc, [1, 1], [1, 1], [0, 0], np.zeros(6), [1, 2], [1, 1], 0.0, pos, hd)
+    want = np.float32([c - 2 * s_, s_ + 2 * c])
+    assert np.array_equal(q, want)
+    other = np.float32([c - s_, 2 * (s_ + c)])
+    assert not np.allclose(q, other, rtol=1e-3)
+
+
+def pin_qknorm_invariants(orc):
+    """Random heads (hd = 8, 3 q heads, 2 k heads), eps = 0: scaling the projection by a power
+    of two changes no bit of q or k; with w = 1 every rotated head has sum of squares hd; a
+    head of +-1 entries has RMS exactly 1, so with w = 1 the stage equals the plain stage
+    (token) bit for bit; an out-of-range position stores nothing."""
+    rng = np.random.default_rng(11)
+    hd, nh, nkv, pos = 8, 3, 2, 5
+    yq = rng.standard_normal(nh * hd)
+    yk = rng.standard_normal(nkv * hd)
+    yv = rng.standard_normal(nkv * hd)
+    w1 = np.ones(hd)
+    wq = rng.uniform(0.5, 1.5, hd)
+    bias = np.zeros((nh + 2 * nkv) * hd)
+    st, q0, k0, v0, _, _ = _qkn(orc, yq, yk, yv, bias, wq, wq[::-1], 0.0, pos, hd, n_ctx=8)
+    for e in (-4, 3):
+        f = 2.0 ** e
+        _, q1, k1, _, _, _ = _qkn(orc, yq * f, yk * f, yv, bias, wq, wq[::-1], 0.0, pos, hd, n_ctx=8)
+        assert np.array_equal(q1, q0) and np.array_equal(k1, k0)
+    _, q2, k2, _, _, _ = _qkn(orc, yq, yk, yv, bias, w1, w1, 0.0, pos, hd, n_ctx=8)
+    for h in range(nh):
+        assert abs(float(np.sum(q2[h * hd:(h + 1) * hd].astype(np.float64) ** 2)) - hd) <= 1e-5
+    sq = np.where(rng.standard_normal(nh * hd) > 0, 1.0, -1.0)
+    sk = np.where(rng.standard_normal(nkv * hd) > 0, 1.0, -1.0)
+    b = rng.standard_normal((nh + 2 * nkv) * hd).astype(np.float32)
+    b[: (nh + nkv) * hd] = 0
+    st, q3, k3, v3, kk3, vv3 = _qkn(orc, sq, sk, yv, b, w1, w1, 0.0, pos, hd, n_ctx=8)
+    kk = np.zeros((8, nkv * hd), np.float32)
+    vv = np.zeros((8, nkv * hd), np.float32)
+    st2, qt, kt, vt = orc.token(np.concatenate([sq, sk, yv]), b, nh, nkv, hd, 1.0e4, 1.0, pos, kk, vv)
+    assert st == st2 == 0
+    assert np.array_equal(q3, qt) and np.array_equal(k3, kt) and np.array_equal(v3, vt)
+    assert np.array_equal(kk3, kk) and np.array_equal(vv3, vv)
+    st, _, _, _, kk4, vv4 = _qkn(orc, yq, yk, yv, bias, wq, wq, 0.0, 8, hd, n_ctx=8)
+    assert st == 1 and not kk4.any() and not vv4.any()
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

@@ -57,6 +57,21 @@ MUTANTS = {
                                "x[c] = (float)((double)h[c] * inv);"),
     "rmsnorm_no_root": ("const double inv = 1.0 / sqrt(ss / (double)H + eps);",
                         "const double inv = 1.0 / (ss / (double)H + eps);"),
+    "qknorm_mean_over_2hd": ("const double inv = 1.0 / sqrt(ss / (double)hd + eps);",
+                             "const double inv = 1.0 / sqrt(ss / (double)(2 * hd) + eps);"),
+    "qknorm_eps_dropped": ("const double inv = 1.0 / sqrt(ss / (double)hd + eps);",
+                           "const double inv = 1.0 / sqrt(ss / (double)hd);"),
+    "qknorm_no_root": ("const double inv = 1.0 / sqrt(ss / (double)hd + eps);",
+                       "const double inv = 1.0 / (ss / (double)hd + eps);"),
+    "qknorm_bias_not_in_rms": ("const double z = y[i] + (double)b[i];", "const double z = y[i];"),
+    "qknorm_weight_index": ("const double n1 = (y[d + half] + (double)b[d + half]) * inv * (double)w[d + half];",
+                            "const double n1 = (y[d + half] + (double)b[d + half]) * inv * (double)w[d];"),
+    "qknorm_k_uses_q_weight": ("qknorm_head(y + nqt + h * hd, bias + nqt + h * hd, k_norm_w,",
+                               "qknorm_head(y + nqt + h * hd, bias + nqt + h * hd, q_norm_w,"),
+    "qknorm_rotation_skipped": ("oracle_rope_pair(n0, n1, 0.0f, 0.0f, pos, f, &out[d], &out[d + half]);",
+                                "oracle_rope_pair(n0, n1, 0.0f, 0.0f, 0, f, &out[d], &out[d + half]);"),
+    "qknorm_k_not_stored": ("for (int i = 0; i < hd; ++i) kv_put(kv_k, kv_is_f16, row + (size_t)(h * hd + i), k_out[h * hd + i]);",
+                            "for (int i = 0; i + 1 < hd; ++i) kv_put(kv_k, kv_is_f16, row + (size_t)(h * hd + i), k_out[h * hd + i]);"),
     "ffn_drops_last_column": ("for (int64_t c = 0; c < H; ++c) {\n                g += (double)rg[c]",
                               "for (int64_t c = 0; c + 1 < H; ++c) {\n                g += (double)rg[c]"),
 }
