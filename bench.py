@@ -185,6 +185,8 @@ def build_model(w: configs.Workload, seed: int):
         keep += [dW, db, dk, dv]
     norms = [torch.from_numpy(synth.norm_weight(seed, l, w.hidden)).to("cuda") for l in range(L)] \
         if w.rmsnorm else None
+    qk_norms = [tuple(torch.from_numpy(a).to("cuda") for a in synth.qk_norm_weights(seed, l, w.head_dim))
+                for l in range(L)] if w.qknorm else None
     layer_plans = [plans[Q.QKV_CLASS_MIXED if l in w.mixed_layers else Q.QKV_CLASS_CONCAT] for l in range(L)]
     h_in = torch.zeros(in_bytes, dtype=torch.uint8).pin_memory()
     h_in[:4].view(torch.int32)[0] = pos
@@ -192,7 +194,8 @@ def build_model(w: configs.Workload, seed: int):
     inbuf.copy_(h_in)
     h_out = torch.empty(L, w.rows, dtype=torch.float32).pin_memory()
     torch.cuda.synchronize()
-    return dict(plans=plans, layer_plans=layer_plans, layers=layers, norms=norms, keep=keep, inbuf=inbuf,
+    return dict(plans=plans, layer_plans=layer_plans, layers=layers, norms=norms, qk_norms=qk_norms, keep=keep,
+                inbuf=inbuf,
                 dpos=dpos, dx=dx, dout=dout, h_in=h_in, h_out=h_out, in_bytes=in_bytes)
 
 
@@ -262,10 +265,14 @@ def oracle_layers_per_s(w: configs.Workload, seed: int, seconds: float, max_laye
         bias = synth.bias(seed, layer, w.rows)
         x = synth.hidden(seed, layer, pos, w.hidden)
         nw = synth.norm_weight(seed, layer, w.hidden) if w.rmsnorm else None
+        qkn = synth.qk_norm_weights(seed, layer, w.head_dim) if w.qknorm else None
         t0 = time.perf_counter()
         if nw is not None:
             x = orc.rmsnorm(x, nw, w.rms_eps)
-        if layer in w.mixed_layers:
+        if qkn is not None:
+            orc.decode_qknorm(W, x, bias, qkn[0], qkn[1], w.qk_eps, w.n_head, w.n_head_kv, w.head_dim, w.theta,
+                              w.freq_scale, pos, kk, vv)
+        elif layer in w.mixed_layers:
             orc.decode_mixed(W[:a], W[a:b], W[b:], x, bias, w.n_head, w.n_head_kv, w.head_dim,
                              w.theta, w.freq_scale, pos, kk, vv)
         else:
@@ -285,19 +292,24 @@ def _oracle_inputs(w, seed: int, layer: int):
                 synth.hidden(seed, 100 + layer, 0, w.hidden))
     return (synth.weight_rows(seed, layer, 0, w.rows, w.hidden, w.w_dtype), synth.bias(seed, layer, w.rows),
             synth.hidden(seed, layer, w.positions[0], w.hidden),
-            synth.norm_weight(seed, layer, w.hidden) if w.rmsnorm else None)
+            synth.norm_weight(seed, layer, w.hidden) if w.rmsnorm else None,
+            synth.qk_norm_weights(seed, layer, w.head_dim) if w.qknorm else None)
 
 
 def _oracle_run(orc, w, layer: int, inp, kv):
     if isinstance(w, configs.FfnWorkload):
         orc.ffn_swiglu(inp[0], inp[1])
         return
-    W, bias, x, nw = inp
+    W, bias, x, nw, qkn = inp
     if nw is not None:
         x = orc.rmsnorm(x, nw, w.rms_eps)
     kk, vv = kv
     a, b = w.nqt, w.nqt + w.nkt
-    if layer in w.mixed_layers:
+    if qkn is not None:
+        # the mixed class computes the same stage from three sections of the same rows
+        orc.decode_qknorm(W, x, bias, qkn[0], qkn[1], w.qk_eps, w.n_head, w.n_head_kv, w.head_dim, w.theta,
+                          w.freq_scale, w.positions[0], kk, vv)
+    elif layer in w.mixed_layers:
         orc.decode_mixed(W[:a], W[a:b], W[b:], x, bias, w.n_head, w.n_head_kv, w.head_dim, w.theta,
                          w.freq_scale, w.positions[0], kk, vv)
     else:
@@ -410,6 +422,8 @@ def workload_config(w: configs.Workload):
             "w_dtype": w.w_dtype, "kv_dtype": w.kv_dtype, "n_ctx": w.n_ctx, "pos": w.positions[0],
             "mixed_layers": "%d-%d" % (w.mixed_layers[0], w.mixed_layers[-1]) if w.mixed_layers else "none",
             "rmsnorm": ("fused in front of each projection, eps %g" % w.rms_eps) if w.rmsnorm else "none (x given)",
+            "qk_norm": ("per-head q/k RMSNorm before RoPE (FusedQkvNorm), weights of %d values, eps %g"
+                        % (w.head_dim, w.qk_eps)) if w.qknorm else "none",
             "l2": ("inputs larger than L2: %.2f GB of weights per step" % (w.n_layers * w.w_bytes() / 1e9))
             if w.n_layers * w.w_bytes() > 4 * L2_BYTES
             else "L2 flushed before every timed step (256 MB written outside the timed events); "
@@ -434,7 +448,13 @@ def native_arm(args, w):
     seed = rank  # each replica runs its own seeded model
     m = build_model(w, seed)
     stream = torch.cuda.Stream()
-    if w.rmsnorm:
+    if w.qknorm:
+        plan0 = m["layer_plans"][0]
+        m["qk_ws"] = torch.zeros(Q.qkv_qknorm_workspace_bytes(plan0) // 4, dtype=torch.int32, device="cuda")
+        graph = Q.qkv_model_graph_create_qknorm(m["layer_plans"], m["layers"], [a for a, _ in m["qk_norms"]],
+                                                [b for _, b in m["qk_norms"]], w.qk_eps, m["dpos"], m["qk_ws"],
+                                                stream)
+    elif w.rmsnorm:
         graph = Q.qkv_model_graph_create_rmsnorm(m["layer_plans"], m["layers"], m["norms"], w.rms_eps, m["dpos"],
                                                  stream)
     else:

@@ -304,6 +304,43 @@ qkv_status qkv_prefill_graph_create(const qkv_plan* const* plans, int32_t n_laye
                                     const qkv_prefill_ptrs* layers, int32_t nt, void* stream,
                                     qkv_graph** out);
 
+/* ---- FusedQkvNorm decode: per-head q / k RMSNorm before the rotation -------- */
+
+/* The Qwen3 variant of the fused stage named on page "06 · Assign + fusion —
+ * every node picks an engine, then patterns fold", §3 (the backend capability
+ * tables: FusedQkvNorm, "q/k per-head norm + the same bias/rope/store").  The
+ * pages give no formula; this library takes the plain reading: after the
+ * bias, each head of q (and of k) is replaced by
+ *   z * w / sqrt( (1/hd) sum_i z_i^2 + eps ),   z = the head's hd biased values,
+ * w = q_norm_w (k_norm_w for k heads, hd floats each, shared by the heads),
+ * then rotated and stored exactly as in qkv_decode_step; v is not normalised.
+ * f32 arithmetic throughout (sum of squares in a fixed order).
+ *
+ * A head's rows are computed by several CTAs, so the stage counts, per head,
+ * the rows already published: the CTA that completes a head normalises,
+ * rotates and stores it.  The counters live in d_workspace, caller-owned
+ * device memory of qkv_qknorm_workspace_bytes() bytes (4-byte aligned) that
+ * must be zero before the first call and is left zero by every completed
+ * call; calls that share a workspace must not overlap on the GPU (one stream).
+ * After a call that set a device status flag, zero it again. */
+qkv_status qkv_qknorm_workspace_bytes(const qkv_plan* plan, size_t* out);
+/* One layer, concat class (w = [wq; wk; wv], bias [R]), arguments otherwise as
+ * qkv_decode_step; eps >= 0.  Rows must be 16-byte aligned (H * element size a
+ * multiple of 16, x and w 16-byte aligned): else UNSUPPORTED.
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+qkv_status qkv_decode_step_qknorm(const qkv_plan* plan, const float* x, const void* w, const float* bias,
+                                  const float* q_norm_w, const float* k_norm_w, float eps,
+                                  const int32_t* d_pos, float* q, float* k, float* v, void* kv_k,
+                                  void* kv_v, void* d_workspace, void* stream);
+/* The whole model in one CUDA graph as qkv_model_graph_create (either layer
+ * class, programmatic dependent launch between layers), every layer through
+ * the FusedQkvNorm stage with its q_norm_w[i] / k_norm_w[i]; the layers share
+ * d_workspace (sized for the layer with the most heads). */
+qkv_status qkv_model_graph_create_qknorm(const qkv_plan* const* plans, int32_t n_layers,
+                                         const qkv_layer_ptrs* layers, const float* const* q_norm_w,
+                                         const float* const* k_norm_w, float eps, const int32_t* d_pos,
+                                         void* d_workspace, void* stream, qkv_graph** out);
+
 /* ---- FusedFFN decode: the FFN's gate|up projection and SwiGLU --------------- */
 
 /* One token of the FFN activation of page "06 · Assign + fusion — every node

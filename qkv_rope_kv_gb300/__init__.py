@@ -128,6 +128,9 @@ def _declare(lib):
         "qkv_ffn_graph_create": ([i32, i32, i32, i32, vp, vp, ctypes.POINTER(vp)], st),
         "qkv_model_graph_run_host": ([vp, vp, vp, sz, vp, vp, sz, vp], st),
         "qkv_model_graph_kernel_count": ([vp, ctypes.POINTER(i32)], st),
+        "qkv_qknorm_workspace_bytes": ([vp, ctypes.POINTER(sz)], st),
+        "qkv_decode_step_qknorm": ([vp, vp, vp, vp, vp, vp, ctypes.c_float] + [vp] * 8, st),
+        "qkv_model_graph_create_qknorm": ([vp, i32, vp, vp, vp, ctypes.c_float, vp, vp, vp, ctypes.POINTER(vp)], st),
         "qkv_model_graph_destroy": ([vp], None),
         "qkv_check_device_error": ([vp, ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(i32)], st),
     }
@@ -330,6 +333,39 @@ def qkv_model_graph_create_rmsnorm(plans, layers, norm_w, norm_eps: float, d_pos
     _check(_lib.qkv_model_graph_create_rmsnorm(arr_plans, n, arr_layers, arr_norm, float(norm_eps), _ptr(d_pos),
                                                _stream(stream), ctypes.byref(h)))
     return ModelGraph(h.value, (plans, layers, norm_w, d_pos))
+
+
+def qkv_qknorm_workspace_bytes(plan: Plan) -> int:
+    out = ctypes.c_size_t()
+    _check(_lib.qkv_qknorm_workspace_bytes(plan.handle, ctypes.byref(out)))
+    return out.value
+
+
+def qkv_decode_step_qknorm(plan: Plan, x, w, bias, q_norm_w, k_norm_w, eps: float, d_pos, q, k, v, kv_k, kv_v,
+                           workspace, stream=None):
+    """qkv_decode_step with per-head q/k RMSNorm (FusedQkvNorm); ``workspace`` is a zeroed device
+    buffer of qkv_qknorm_workspace_bytes(plan) bytes, left zeroed."""
+    _check(_lib.qkv_decode_step_qknorm(plan.handle, _ptr(x), _ptr(w), _ptr(bias), _ptr(q_norm_w), _ptr(k_norm_w),
+                                       float(eps), _ptr(d_pos), _ptr(q), _ptr(k), _ptr(v), _ptr(kv_k), _ptr(kv_v),
+                                       _ptr(workspace), _stream(stream)))
+
+
+def qkv_model_graph_create_qknorm(plans, layers, q_norm_w, k_norm_w, eps: float, d_pos, workspace,
+                                  stream) -> ModelGraph:
+    """The FusedQkvNorm model graph: q_norm_w[i] / k_norm_w[i] per layer, one shared workspace."""
+    n = len(plans)
+    assert len(layers) == n and len(q_norm_w) == n and len(k_norm_w) == n
+    arr_plans = (ctypes.c_void_p * n)(*[p.handle for p in plans])
+    arr_layers = (qkv_layer_ptrs * n)()
+    for i, L in enumerate(layers):
+        for name, _ in qkv_layer_ptrs._fields_:
+            setattr(arr_layers[i], name, _ptr(L.get(name)))
+    arr_q = (ctypes.c_void_p * n)(*[_ptr(t) for t in q_norm_w])
+    arr_k = (ctypes.c_void_p * n)(*[_ptr(t) for t in k_norm_w])
+    h = ctypes.c_void_p()
+    _check(_lib.qkv_model_graph_create_qknorm(arr_plans, n, arr_layers, arr_q, arr_k, float(eps), _ptr(d_pos),
+                                              _ptr(workspace), _stream(stream), ctypes.byref(h)))
+    return ModelGraph(h.value, (plans, layers, q_norm_w, k_norm_w, d_pos, workspace))
 
 
 def qkv_prefill_graph_create(plans, layers, nt: int, stream) -> ModelGraph:

@@ -29,6 +29,8 @@ class Workload:
     nt: int = 1             # tokens per step (prefill when > 1)
     rmsnorm: bool = False   # decode input is the hidden state; its RMSNorm runs in the projection kernel
     rms_eps: float = 1.0e-6
+    qknorm: bool = False    # FusedQkvNorm: every q / k head RMS-normalised (weights of hd values) before RoPE
+    qk_eps: float = 1.0e-6
 
     @property
     def nqt(self) -> int:
@@ -51,7 +53,8 @@ class Workload:
     def algo_bytes_per_layer(self) -> int:
         """Bytes one decode layer must move: W, x, bias read; q|k|v and one cache row per region written."""
         return (self.w_bytes() + 4 * self.hidden + 4 * self.rows + 4 * self.rows
-                + 2 * self.nkt * self.kv_elem_bytes() + (4 * self.hidden if self.rmsnorm else 0))
+                + 2 * self.nkt * self.kv_elem_bytes() + (4 * self.hidden if self.rmsnorm else 0)
+                + (2 * 4 * self.head_dim if self.qknorm else 0))
 
 
 QWEN05_SINGLE = Workload("qwen2.5-0.5b-single-layer", 896, 14, 2, 64, "f32", "f32", 512, 1, (17,))
@@ -70,8 +73,14 @@ QWEN7B_NORM = Workload("qwen2.5-7b-28layer-rmsnorm", 3584, 28, 4, 128, "bf16", "
 QWEN14B_NORM = Workload("qwen2.5-14b-48layer-mixed-rmsnorm", 5120, 40, 8, 128, "bf16", "f16", 4096, 48, (3254,),
                         mixed_layers=tuple(range(24, 48)), rmsnorm=True)
 
+# Qwen3-14B attention input (H 5120, 40 q / 8 kv heads of 128, per-head q/k norm), the model
+# family the pages name for FusedQkvNorm; synthetic weights, and a bias (the stage's own op
+# carries one; zero-free here so the bias path stays exercised).
+QWEN3_14B_QKNORM = Workload("qwen3-14b-48layer-qknorm", 5120, 40, 8, 128, "bf16", "f16", 4096, 48, (3254,),
+                            qknorm=True)
+
 WORKLOADS = {w.name: w for w in (QWEN05_SINGLE, QWEN05_SWEEP, QWEN7B, QWEN14B, QWEN14B_PREFILL, QWEN7B_NORM,
-                                 QWEN14B_NORM)}
+                                 QWEN14B_NORM, QWEN3_14B_QKNORM)}
 
 
 @dataclass(frozen=True)

@@ -704,19 +704,20 @@ constexpr int kBlkPairs = QKV_DECODE_BLOCK_PAIRS;  // rows per stage (one contig
 
 // What the block ring computes after the projection.
 enum BlockEpilogue {
-    kEpiQkv = 0,     // bias, neox RoPE on q/k, KV-cache store (units: neox pairs of a head, v rows)
-    kEpiSwiglu = 1,  // silu(gate) * up (units: rows i of the gate half with rows nf + i)
+    kEpiQkv = 0,      // bias, neox RoPE on q/k, KV-cache store (units: neox pairs of a head, v rows)
+    kEpiSwiglu = 1,   // silu(gate) * up (units: rows i of the gate half with rows nf + i)
+    kEpiQkvNorm = 2,  // as kEpiQkv with each q / k head RMS-normalised before its rotation
 };
 
 template <int EPI>
 __device__ __forceinline__ int blk_unit_count(const DecodeParams& p) {
-    if constexpr (EPI == kEpiQkv) return unit_count<kBlkPairs>(p.nqt, p.nkt, p.hd);
+    if constexpr (EPI != kEpiSwiglu) return unit_count<kBlkPairs>(p.nqt, p.nkt, p.hd);
     else return (p.nf + kBlkPairs - 1) / kBlkPairs;
 }
 
 template <int EPI>
 __device__ __forceinline__ Unit blk_unit(int u, const DecodeParams& p) {
-    if constexpr (EPI == kEpiQkv) {
+    if constexpr (EPI != kEpiSwiglu) {
         return unit_info<kBlkPairs>(u, p.nqt, p.nkt, p.hd);
     } else {
         Unit t;
@@ -731,6 +732,34 @@ __device__ __forceinline__ Unit blk_unit(int u, const DecodeParams& p) {
 // SwiGLU of one (gate, up) pair, each step rounded to f32: silu(g) = g / (1 + e^-g).
 __device__ __forceinline__ float swiglu(float g, float u) {
     return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+}
+
+// FusedQkvNorm: finish head hh (q heads first, then k heads) whose biased values
+// z = y + b sit in the output section, written by the CTAs that computed its rows.  One
+// warp: sum of z^2 (lane l takes elements l, l + 32, ... in order, then a xor butterfly),
+// inv = 1 / sqrt(sum / hd + eps), then pair d (lane-strided) becomes
+// (z_d inv w_d, z_{d+hd/2} inv w_{d+hd/2}), rotated and stored as in the plain stage.
+// The values are read at L2 (ld.global.cg): other SMs wrote them.
+__device__ __forceinline__ void qknorm_finish_head(const DecodeParams& p, int hh, int pos, bool store,
+                                                   const float* freq_s, int lane) {
+    const int hd = p.hd, half = hd >> 1;
+    const int nhq = p.nqt / hd;
+    const int sec = hh < nhq ? 0 : 1;
+    const int base = (sec ? hh - nhq : hh) * hd;
+    const float* z = p.out[sec] + base;
+    const float* w = p.qk_norm_w[sec];
+    float ss = 0.f;
+    for (int i = lane; i < hd; i += 32) {
+        const float v = __ldcg(z + i);
+        ss = __fmaf_rn(v, v, ss);
+    }
+    ss = warp_sum(ss);
+    const float inv = __fdiv_rn(1.f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(hd)), p.qk_eps)));
+    for (int d = lane; d < half; d += 32) {
+        const float n0 = __fmul_rn(__fmul_rn(__ldcg(z + d), inv), __ldg(w + d));
+        const float n1 = __fmul_rn(__fmul_rn(__ldcg(z + d + half), inv), __ldg(w + d + half));
+        epi_qk_rot(p, sec, base + d, base + d + half, n0, n1, pos, freq_s[d], store);
+    }
 }
 
 // Block ring: a unit of kBlkPairs neox pairs has two row blocks, (h*hd + d0 ..)
@@ -811,7 +840,7 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
     // ---- consumers ----
     // Biases are parameters, not outputs of an earlier kernel: stage this CTA's
     // share before the dependency wait, so no global load sits in the item loop.
-    if (MODE == kFused && EPI == kEpiQkv) {
+    if (MODE == kFused && EPI != kEpiSwiglu) {
         const int nb = (u_end - u_begin) * 2 * kBlkPairs;
         for (int e = threadIdx.x; e < nb; e += kGroups * 32) {
             const int j = e % kBlkPairs, blk = (e / kBlkPairs) & 1, ul = e / (2 * kBlkPairs);
@@ -824,14 +853,14 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
     {
         const int tid = threadIdx.x, nthr = kGroups * 32;
         stage_input<WT, true>(p, xs4, tid, nthr);
-        if (EPI == kEpiQkv)
+        if (EPI != kEpiSwiglu)
             for (int i = tid; i < (p.hd >> 1); i += nthr) freq_s[i] = p.inv_freq[i];
     }
     named_barrier_sync(1, kGroups * 32);
     const float inv = norm_inv(p, kGroups * 32);
-    const int pos = (MODE == kFused && EPI == kEpiQkv) ? *p.pos : 0;
+    const int pos = (MODE == kFused && EPI != kEpiSwiglu) ? *p.pos : 0;
     const bool store = pos_ok(pos, p.n_ctx);
-    if (MODE == kFused && EPI == kEpiQkv && !store && blockIdx.x == 0 && threadIdx.x == 0) flag_bad_pos(pos);
+    if (MODE == kFused && EPI != kEpiSwiglu && !store && blockIdx.x == 0 && threadIdx.x == 0) flag_bad_pos(pos);
 
     for (int i = warp; i < n; i += kGroups) {
         const int st = i % stages;
@@ -885,6 +914,9 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
             if (lane < t.n) p.out[t.sec][rb + lane] = yl;
         } else if (t.sec == 2) {
             if (lane < t.n) epi_v_elem_b(p, rb + lane, yl, bias_s[e], pos, store);
+        } else if constexpr (EPI == kEpiQkvNorm) {
+            // a head's norm needs all of its rows: publish z = y + b; the head's last CTA finishes it
+            if (lane < t.n) p.out[t.sec][rb + lane] = __fadd_rn(yl, bias_s[e]);
         } else {
             const float yb = lane < t.n ? __fadd_rn(yl, bias_s[e]) : 0.f;
             if (lane < t.n) res[e] = yb;
@@ -902,6 +934,30 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
                 const float o = static_cast<volatile float*>(res)[e + (blk ? -kBlkPairs : kBlkPairs)];
                 const int r0 = t.r + lane;
                 epi_qk_rot(p, t.sec, r0, r0 + t.off, blk ? o : yb, blk ? yb : o, pos, freq_s[r0 % p.hd], store);
+            }
+        }
+    }
+    if constexpr (EPI == kEpiQkvNorm && MODE == kFused) {
+        // Every raw q / k value of this CTA is written; count this CTA's units into each
+        // head it touched.  The CTA that completes a head's count finishes that head.
+        named_barrier_sync(1, kGroups * 32);
+        const int per_head = ((p.hd >> 1) + kBlkPairs - 1) / kBlkPairs;
+        const int qk_end = min(u_end, (p.nqt / p.hd + p.nkt / p.hd) * per_head);
+        if (u_begin < qk_end) {
+            const int h0 = u_begin / per_head, h1 = (qk_end - 1) / per_head;
+            for (int hh = h0 + warp; hh <= h1; hh += kGroups) {
+                const int mine = min(qk_end, (hh + 1) * per_head) - max(u_begin, hh * per_head);
+                int last = 0;
+                if (lane == 0) {
+                    __threadfence();  // this CTA's values of head hh before its count
+                    last = atomicAdd(&p.head_cnt[hh], static_cast<unsigned int>(mine)) + mine ==
+                           static_cast<unsigned int>(per_head);
+                    if (last) {
+                        p.head_cnt[hh] = 0u;  // every contributor has counted: ready for the next launch
+                        __threadfence();      // the other CTAs' values of head hh after their counts
+                    }
+                }
+                if (__shfl_sync(0xffffffffu, last, 0)) qknorm_finish_head(p, hh, pos, store, freq_s, lane);
             }
         }
     }
@@ -1073,7 +1129,8 @@ cudaError_t launch_decode_blk(const DecodeParams& p, int ctas_per_sm, int smem_k
     const size_t row = static_cast<size_t>(p.H) * sizeof(WT);
     const uint32_t stage_bytes = static_cast<uint32_t>((kBlkPairs * row + 127) / 128 * 128);
     const uint32_t x_bytes = static_cast<uint32_t>((static_cast<size_t>(p.H) * 4 + 127) / 128 * 128);
-    const int units = EPI == kEpiQkv ? unit_count<kBlkPairs>(p.nqt, p.nkt, p.hd) : (p.nf + kBlkPairs - 1) / kBlkPairs;
+    const int units =
+        EPI != kEpiSwiglu ? unit_count<kBlkPairs>(p.nqt, p.nkt, p.hd) : (p.nf + kBlkPairs - 1) / kBlkPairs;
     const int ctas_max = sm_count() * ctas_per_sm;
     const int grid = units < ctas_max ? units : ctas_max;
     const int skew = pdl ? kChainSkewBlock : 0;
@@ -1155,7 +1212,25 @@ cudaError_t launch_ffn_t(const DecodeParams& p, bool pdl, cudaStream_t stream) {
     return launched ? cudaSuccess : cudaErrorNotSupported;
 }
 
+template <typename WT>
+cudaError_t launch_qknorm_t(const DecodeParams& p, bool pdl, cudaStream_t stream) {
+    const size_t row = static_cast<size_t>(p.H) * sizeof(WT);
+    bool launched = false;
+    const cudaError_t e =
+        row >= kSmallRowBytes
+            ? launch_decode_blk<WT, kFused, kGroupsLarge, kEpiQkvNorm>(p, QKV_DECODE_LARGE_CTAS,
+                                                                      QKV_DECODE_LARGE_SMEM_KB, pdl, stream, launched)
+            : launch_decode_blk<WT, kFused, kGroupsSmall, kEpiQkvNorm>(p, QKV_DECODE_SMALL_CTAS,
+                                                                      QKV_DECODE_SMALL_SMEM_KB, pdl, stream, launched);
+    if (e != cudaSuccess) return e;
+    return launched ? cudaSuccess : cudaErrorNotSupported;
+}
+
 }  // namespace
+
+cudaError_t launch_qknorm(const DecodeParams& p, int w_dtype, bool pdl, cudaStream_t stream) {
+    return w_dtype == QKV_BF16 ? launch_qknorm_t<uint16_t>(p, pdl, stream) : launch_qknorm_t<float>(p, pdl, stream);
+}
 
 cudaError_t launch_ffn(const DecodeParams& p, int w_dtype, bool pdl, cudaStream_t stream) {
     return w_dtype == QKV_BF16 ? launch_ffn_t<uint16_t>(p, pdl, stream) : launch_ffn_t<float>(p, pdl, stream);

@@ -107,6 +107,45 @@ qkv_status run_decode(const qkv_plan* plan, const float* x, const void* const w[
     return QKV_OK;
 }
 
+// FusedQkvNorm: the fused stage with per-head q / k RMSNorm; rows must be 16-byte aligned.
+qkv_status check_qknorm_args(const qkv_plan* plan, const float* x, const void* const w[3], const float* q_norm_w,
+                             const float* k_norm_w, float eps, const void* d_workspace) {
+    REQUIRE(q_norm_w && k_norm_w, "q_norm_w or k_norm_w is null");
+    REQUIRE(eps >= 0.f && eps == eps, "eps must be a number >= 0");
+    REQUIRE(d_workspace, "d_workspace is null");
+    REQUIRE((reinterpret_cast<uintptr_t>(d_workspace) & 3u) == 0, "d_workspace must be 4-byte aligned");
+    if (!use_vec(plan, x, w))
+        return fail(QKV_ERR_UNSUPPORTED, "FusedQkvNorm needs 16-byte aligned x and weight rows "
+                                         "(hidden * element size a multiple of 16)");
+    return QKV_OK;
+}
+
+qkv_status run_qknorm(const qkv_plan* plan, const float* x, const void* const w[3], const float* const b[3],
+                      const float* q_norm_w, const float* k_norm_w, float eps, const int32_t* d_pos, float* q,
+                      float* k, float* v, void* kv_k, void* kv_v, void* d_workspace, bool pdl, cudaStream_t s) {
+    DecodeParams p = base_params(plan);
+    p.x = x;
+    for (int i = 0; i < 3; ++i) {
+        p.w[i] = w[i];
+        p.bias[i] = b[i];
+    }
+    p.out[0] = q;
+    p.out[1] = k;
+    p.out[2] = v;
+    p.kv_k = kv_k;
+    p.kv_v = kv_v;
+    p.pos = d_pos;
+    p.qk_norm_w[0] = q_norm_w;
+    p.qk_norm_w[1] = k_norm_w;
+    p.qk_eps = eps;
+    p.head_cnt = static_cast<unsigned int*>(d_workspace);
+    const cudaError_t e = launch_qknorm(p, plan->d.w_dtype, pdl, s);
+    if (e == cudaErrorNotSupported)
+        return fail(QKV_ERR_UNSUPPORTED, "hidden %d leaves no room for the ring", plan->d.hidden);
+    if (e != cudaSuccess) return cuda_fail(e, "FusedQkvNorm kernel launch");
+    return QKV_OK;
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ library
@@ -243,6 +282,32 @@ extern "C" qkv_status qkv_decode_step_rmsnorm(const qkv_plan* plan, const float*
     if (st != QKV_OK) return st;
     return run_decode(plan, h, ws, bs, d_pos, q, k, v, kv_k, kv_v, false, static_cast<cudaStream_t>(stream),
                       norm_w, norm_eps);
+}
+
+extern "C" qkv_status qkv_qknorm_workspace_bytes(const qkv_plan* plan, size_t* out) {
+    REQUIRE(plan && out, "null argument");
+    *out = static_cast<size_t>(plan->d.n_head + plan->d.n_head_kv) * sizeof(uint32_t);
+    return QKV_OK;
+}
+
+extern "C" qkv_status qkv_decode_step_qknorm(const qkv_plan* plan, const float* x, const void* w, const float* bias,
+                                             const float* q_norm_w, const float* k_norm_w, float eps,
+                                             const int32_t* d_pos, float* q, float* k, float* v, void* kv_k,
+                                             void* kv_v, void* d_workspace, void* stream) {
+    REQUIRE(plan, "plan is null");
+    REQUIRE(plan->d.layer_class == QKV_CLASS_CONCAT, "qkv_decode_step_qknorm needs a concat-class plan");
+    REQUIRE(w && bias, "w or bias is null");
+    const size_t es = elem_size(plan->d.w_dtype);
+    const char* wb = static_cast<const char*>(w);
+    const void* ws[3] = {wb, wb + plan->nqt * plan->d.hidden * es,
+                         wb + (plan->nqt + plan->nkt) * plan->d.hidden * es};
+    const float* bs[3] = {bias, bias + plan->nqt, bias + plan->nqt + plan->nkt};
+    qkv_status st = check_decode_ptrs(plan, x, ws, bs, d_pos, q, k, v, kv_k, kv_v);
+    if (st != QKV_OK) return st;
+    st = check_qknorm_args(plan, x, ws, q_norm_w, k_norm_w, eps, d_workspace);
+    if (st != QKV_OK) return st;
+    return run_qknorm(plan, x, ws, bs, q_norm_w, k_norm_w, eps, d_pos, q, k, v, kv_k, kv_v, d_workspace, false,
+                      static_cast<cudaStream_t>(stream));
 }
 
 extern "C" qkv_status qkv_decode_step_mixed(const qkv_plan* plan, const float* x, const void* wq,
@@ -479,6 +544,70 @@ extern "C" qkv_status qkv_model_graph_create_rmsnorm(const qkv_plan* const* plan
         REQUIRE(aligned16(norm_w[i]), "norm weight of layer %d must be 16-byte aligned", i);
     }
     return model_graph_create(plans, n_layers, layers, norm_w, norm_eps, d_pos, stream, out);
+}
+
+namespace {
+// Section pointers of a model-graph layer (both classes).
+void layer_sections(const qkv_plan* p, const qkv_layer_ptrs& L, const void* ws[3], const float* bs[3]) {
+    if (p->d.layer_class == QKV_CLASS_CONCAT) {
+        const size_t es = elem_size(p->d.w_dtype);
+        const char* wb = static_cast<const char*>(L.w);
+        ws[0] = wb;
+        ws[1] = wb + p->nqt * p->d.hidden * es;
+        ws[2] = wb + (p->nqt + p->nkt) * p->d.hidden * es;
+        bs[0] = L.bias;
+        bs[1] = L.bias + p->nqt;
+        bs[2] = L.bias + p->nqt + p->nkt;
+    } else {
+        ws[0] = L.wq;
+        ws[1] = L.wk;
+        ws[2] = L.wv;
+        bs[0] = L.bias_q;
+        bs[1] = L.bias_k;
+        bs[2] = L.bias_v;
+    }
+}
+}  // namespace
+
+extern "C" qkv_status qkv_model_graph_create_qknorm(const qkv_plan* const* plans, int32_t n_layers,
+                                                    const qkv_layer_ptrs* layers, const float* const* q_norm_w,
+                                                    const float* const* k_norm_w, float eps, const int32_t* d_pos,
+                                                    void* d_workspace, void* stream, qkv_graph** out) {
+    REQUIRE(out, "out is null");
+    *out = nullptr;
+    REQUIRE(plans && layers && d_pos && q_norm_w && k_norm_w, "null argument");
+    REQUIRE(n_layers >= 1, "n_layers must be >= 1");
+    REQUIRE(stream, "capture needs a non-default stream");
+    for (int32_t i = 0; i < n_layers; ++i) {
+        const qkv_plan* p = plans[i];
+        const qkv_layer_ptrs& L = layers[i];
+        REQUIRE(p, "plan of layer %d is null", i);
+        if (p->d.layer_class == QKV_CLASS_CONCAT) {
+            REQUIRE(L.w && L.bias, "layer %d (concat): w or bias is null", i);
+        } else {
+            REQUIRE(L.wq && L.wk && L.wv && L.bias_q && L.bias_k && L.bias_v,
+                    "layer %d (mixed): a weight or bias pointer is null", i);
+        }
+        const void* ws[3];
+        const float* bs[3];
+        layer_sections(p, L, ws, bs);
+        qkv_status st = check_decode_ptrs(p, L.x, ws, bs, d_pos, L.q, L.k, L.v, L.kv_k, L.kv_v);
+        if (st == QKV_OK) st = check_qknorm_args(p, L.x, ws, q_norm_w[i], k_norm_w[i], eps, d_workspace);
+        if (st != QKV_OK) return fail(st, "layer %d: %s", i, g_last_error.c_str());
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamBeginCapture");
+    qkv_status st = QKV_OK;
+    for (int32_t i = 0; i < n_layers && st == QKV_OK; ++i) {
+        const qkv_layer_ptrs& L = layers[i];
+        const void* ws[3];
+        const float* bs[3];
+        layer_sections(plans[i], L, ws, bs);
+        st = run_qknorm(plans[i], L.x, ws, bs, q_norm_w[i], k_norm_w[i], eps, d_pos, L.q, L.k, L.v, L.kv_k, L.kv_v,
+                        d_workspace, i > 0, s);
+    }
+    return finish_capture(s, st, out);
 }
 
 namespace {

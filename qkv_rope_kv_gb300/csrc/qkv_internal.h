@@ -28,6 +28,9 @@ struct DecodeParams {
     int32_t nf;             // FusedFFN: rows per half of the gate|up weight (0 for the QKV stage)
     const float* norm_w;    // RMSNorm weight [H]: x is then the hidden state h, normalised in-kernel
     float norm_eps;         // RMSNorm epsilon
+    const float* qk_norm_w[2];  // FusedQkvNorm: per-head norm weights of q and k [hd] each
+    float qk_eps;               // FusedQkvNorm epsilon
+    unsigned int* head_cnt;     // FusedQkvNorm: per-head completion counters [nh + nkv], zero between launches
     float inv_freq[QKV_MAX_HEAD_DIM / 2];
 };
 
@@ -46,6 +49,11 @@ cudaError_t device_status_read(cudaStream_t stream, uint32_t* flags, int32_t* ba
 // weight p.w[0] [2 nf x H] into p.out[0] [nf]; rows must be 16-byte aligned.
 // Returns cudaErrorNotSupported when no ring shape fits the hidden size.
 cudaError_t launch_ffn(const DecodeParams& p, int w_dtype, bool pdl, cudaStream_t stream);
+// FusedQkvNorm decode: the fused stage with each q and k head RMS-normalised (weights
+// p.qk_norm_w, epsilon p.qk_eps) after its bias and before its rotation; p.head_cnt is a
+// zeroed workspace of nh + nkv counters, left zeroed.  Rows must be 16-byte aligned.
+// Returns cudaErrorNotSupported when no ring shape fits the hidden size.
+cudaError_t launch_qknorm(const DecodeParams& p, int w_dtype, bool pdl, cudaStream_t stream);
 
 // prefill_tcgen05.cu
 struct PrefillParams {

@@ -133,6 +133,12 @@ def norm_weight(seed: int, layer: int, h: int) -> np.ndarray:
     return (np.float32(1.0) + normal_f32(seed, T_NORM, layer, 0, h, NORM_SIGMA)).astype(np.float32)
 
 
+def qk_norm_weights(seed: int, layer: int, hd: int):
+    """Per-head q and k norm weights of a layer (hd values each, 1 + N(0, 0.1)): the
+    norm-weight streams 1000 + 2 layer and 1001 + 2 layer."""
+    return norm_weight(seed, 1000 + 2 * layer, hd), norm_weight(seed, 1001 + 2 * layer, hd)
+
+
 def bias(seed: int, layer: int, n_rows: int) -> np.ndarray:
     """Concatenated bq|bk|bv, float32, ~N(0, 0.1)."""
     return normal_f32(seed, T_BIAS, layer, 0, n_rows, BIAS_SIGMA)

@@ -194,3 +194,41 @@ def test_rmsnorm_guards(lib):
     assert g(plans, 1, layers, None, ctypes.c_float(1e-6), 16, 16, ctypes.byref(h)) == q.QKV_ERR_INVALID_ARG
     assert g(plans, 1, layers, norms, ctypes.c_float(1e-6), 16, 16, ctypes.byref(h)) == q.QKV_ERR_INVALID_ARG
 
+
+
+def test_qknorm_guards(lib):
+    """FusedQkvNorm arguments are validated on the host before any CUDA call."""
+    fake = 16 * 64  # 16-byte aligned stand-in address; nothing is dereferenced on failure
+    p = q.qkv_plan_create(64, 2, 1, 8, 1e4, 16)
+    assert q.qkv_qknorm_workspace_bytes(p) == 3 * 4
+    f = lib.qkv_decode_step_qknorm
+    args = [p.handle, fake, fake, fake, fake, fake, ctypes.c_float(1e-6), fake, fake, fake, fake, fake, fake, fake,
+            None]
+    for i, bad in ((4, None), (5, None), (13, None), (13, fake + 2)):
+        a = list(args)
+        a[i] = bad
+        assert f(*a) == q.QKV_ERR_INVALID_ARG, i
+    for eps in (-1.0, float("nan")):
+        a = list(args)
+        a[6] = ctypes.c_float(eps)
+        assert f(*a) == q.QKV_ERR_INVALID_ARG
+    a = list(args)
+    a[1] = fake + 4  # x not 16-byte aligned: no ring form
+    assert f(*a) == q.QKV_ERR_UNSUPPORTED
+    mixed = q.qkv_plan_create(64, 2, 1, 8, 1e4, 16, layer_class=q.QKV_CLASS_MIXED)
+    a = list(args)
+    a[0] = mixed.handle
+    assert f(*a) == q.QKV_ERR_INVALID_ARG
+    h = ctypes.c_void_p()
+    plans = (ctypes.c_void_p * 1)(p.handle)
+    layers = (q.qkv_layer_ptrs * 1)()
+    for name, _ in q.qkv_layer_ptrs._fields_:
+        setattr(layers[0], name, fake)
+    norms = (ctypes.c_void_p * 1)(fake)
+    g = lib.qkv_model_graph_create_qknorm
+    assert g(plans, 1, layers, norms, norms, ctypes.c_float(1e-6), fake, None, fake, ctypes.byref(h)) == \
+        q.QKV_ERR_INVALID_ARG
+    assert g(plans, 1, layers, None, norms, ctypes.c_float(1e-6), fake, fake, fake, ctypes.byref(h)) == \
+        q.QKV_ERR_INVALID_ARG
+    assert g(plans, 0, layers, norms, norms, ctypes.c_float(1e-6), fake, fake, fake, ctypes.byref(h)) == \
+        q.QKV_ERR_INVALID_ARG
