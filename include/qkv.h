@@ -332,6 +332,26 @@ qkv_status qkv_decode_step_qknorm(const qkv_plan* plan, const float* x, const vo
                                   const float* q_norm_w, const float* k_norm_w, float eps,
                                   const int32_t* d_pos, float* q, float* k, float* v, void* kv_k,
                                   void* kv_v, void* d_workspace, void* stream);
+/* qkv_decode_step_qknorm for callers that cannot allocate device memory
+ * themselves (for instance code running inside an allocator callback or a
+ * memory pool that must not grow, or a host that has handed every byte of the
+ * GPU to another owner): the per-head counters live in a fixed array inside
+ * the library (1024 counters, 4 KB, reserved on every device that loads the
+ * library until the process exits), so nothing is allocated, by the caller or
+ * by the library.  The pages have no counterpart of this entry point.
+ *   - At most 1024 q + kv heads (nh + nkv); larger plans get INVALID_ARG.
+ *   - The first call on a device looks up the array's device address there
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture on the device.
+ *   - Every call clears the counters it uses (an asynchronous memset on
+ *     `stream`) and shares the one array with every other call on the device:
+ *     calls that may overlap on the GPU (different streams, or graph replays
+ *     running concurrently) race on it.  Run them in one stream.
+ * Arguments, results and other errors as qkv_decode_step_qknorm. */
+qkv_status qkv_decode_step_qknorm_noalloc(const qkv_plan* plan, const float* x, const void* w, const float* bias,
+                                          const float* q_norm_w, const float* k_norm_w, float eps,
+                                          const int32_t* d_pos, float* q, float* k, float* v, void* kv_k,
+                                          void* kv_v, void* stream);
 /* The whole model in one CUDA graph as qkv_model_graph_create (either layer
  * class, programmatic dependent launch between layers), every layer through
  * the FusedQkvNorm stage with its q_norm_w[i] / k_norm_w[i]; the layers share

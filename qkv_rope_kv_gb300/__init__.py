@@ -130,6 +130,7 @@ def _declare(lib):
         "qkv_model_graph_kernel_count": ([vp, ctypes.POINTER(i32)], st),
         "qkv_qknorm_workspace_bytes": ([vp, ctypes.POINTER(sz)], st),
         "qkv_decode_step_qknorm": ([vp, vp, vp, vp, vp, vp, ctypes.c_float] + [vp] * 8, st),
+        "qkv_decode_step_qknorm_noalloc": ([vp, vp, vp, vp, vp, vp, ctypes.c_float] + [vp] * 7, st),
         "qkv_model_graph_create_qknorm": ([vp, i32, vp, vp, vp, ctypes.c_float, vp, vp, vp, ctypes.POINTER(vp)], st),
         "qkv_model_graph_destroy": ([vp], None),
         "qkv_check_device_error": ([vp, ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(i32)], st),
@@ -348,6 +349,15 @@ def qkv_decode_step_qknorm(plan: Plan, x, w, bias, q_norm_w, k_norm_w, eps: floa
     _check(_lib.qkv_decode_step_qknorm(plan.handle, _ptr(x), _ptr(w), _ptr(bias), _ptr(q_norm_w), _ptr(k_norm_w),
                                        float(eps), _ptr(d_pos), _ptr(q), _ptr(k), _ptr(v), _ptr(kv_k), _ptr(kv_v),
                                        _ptr(workspace), _stream(stream)))
+
+
+def qkv_decode_step_qknorm_noalloc(plan: Plan, x, w, bias, q_norm_w, k_norm_w, eps: float, d_pos, q, k, v, kv_k,
+                                   kv_v, stream=None):
+    """qkv_decode_step_qknorm without a workspace: the counters are the library's own fixed
+    device array (at most 1024 q + kv heads; calls sharing it must not overlap on the GPU)."""
+    _check(_lib.qkv_decode_step_qknorm_noalloc(plan.handle, _ptr(x), _ptr(w), _ptr(bias), _ptr(q_norm_w),
+                                               _ptr(k_norm_w), float(eps), _ptr(d_pos), _ptr(q), _ptr(k), _ptr(v),
+                                               _ptr(kv_k), _ptr(kv_v), _stream(stream)))
 
 
 def qkv_model_graph_create_qknorm(plans, layers, q_norm_w, k_norm_w, eps: float, d_pos, workspace,

@@ -28,6 +28,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "epilogue_math.cuh"
 #include "ptx_sync.cuh"
 #include "qkv_internal.h"
@@ -1230,6 +1232,31 @@ cudaError_t launch_qknorm_t(const DecodeParams& p, bool pdl, cudaStream_t stream
 
 cudaError_t launch_qknorm(const DecodeParams& p, int w_dtype, bool pdl, cudaStream_t stream) {
     return w_dtype == QKV_BF16 ? launch_qknorm_t<uint16_t>(p, pdl, stream) : launch_qknorm_t<float>(p, pdl, stream);
+}
+
+// Library-owned per-head counters for callers that cannot allocate device memory: a
+// fixed array in the module's global memory, present on every device that loads the
+// library, holding kQknormStaticHeads counters (4 KB).
+static __device__ __align__(256) unsigned int g_qknorm_static_counters[kQknormStaticHeads];
+
+cudaError_t qknorm_static_workspace(unsigned int** out) {
+    // Host code cannot use the array's name as a device address: look the address up
+    // once per device, with that device current, and reuse it.
+    static std::mutex mu;
+    static unsigned int* addr[kQknormMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kQknormMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_qknorm_static_counters);
+        if (e != cudaSuccess) return e;
+        addr[dev] = static_cast<unsigned int*>(p);
+    }
+    *out = addr[dev];
+    return cudaSuccess;
 }
 
 cudaError_t launch_ffn(const DecodeParams& p, int w_dtype, bool pdl, cudaStream_t stream) {

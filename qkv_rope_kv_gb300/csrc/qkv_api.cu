@@ -310,6 +310,37 @@ extern "C" qkv_status qkv_decode_step_qknorm(const qkv_plan* plan, const float* 
                       static_cast<cudaStream_t>(stream));
 }
 
+extern "C" qkv_status qkv_decode_step_qknorm_noalloc(const qkv_plan* plan, const float* x, const void* w,
+                                                     const float* bias, const float* q_norm_w,
+                                                     const float* k_norm_w, float eps, const int32_t* d_pos,
+                                                     float* q, float* k, float* v, void* kv_k, void* kv_v,
+                                                     void* stream) {
+    REQUIRE(plan, "plan is null");
+    REQUIRE(plan->d.n_head + plan->d.n_head_kv <= kQknormStaticHeads,
+            "qkv_decode_step_qknorm_noalloc handles at most %d q + kv heads (this plan has %d); use "
+            "qkv_decode_step_qknorm with a workspace", kQknormStaticHeads, plan->d.n_head + plan->d.n_head_kv);
+    REQUIRE(plan->d.layer_class == QKV_CLASS_CONCAT, "qkv_decode_step_qknorm_noalloc needs a concat-class plan");
+    REQUIRE(w && bias, "w or bias is null");
+    const size_t es = elem_size(plan->d.w_dtype);
+    const char* wb = static_cast<const char*>(w);
+    const void* ws[3] = {wb, wb + plan->nqt * plan->d.hidden * es,
+                         wb + (plan->nqt + plan->nkt) * plan->d.hidden * es};
+    const float* bs[3] = {bias, bias + plan->nqt, bias + plan->nqt + plan->nkt};
+    qkv_status st = check_decode_ptrs(plan, x, ws, bs, d_pos, q, k, v, kv_k, kv_v);
+    if (st != QKV_OK) return st;
+    unsigned int* counters = nullptr;
+    cudaError_t e = qknorm_static_workspace(&counters);
+    if (e != cudaSuccess) return cuda_fail(e, "looking up the library's FusedQkvNorm counters");
+    st = check_qknorm_args(plan, x, ws, q_norm_w, k_norm_w, eps, counters);
+    if (st != QKV_OK) return st;
+    // The counters must start at zero; a completed call leaves them at zero, an
+    // interrupted one may not, so every call clears its share on its own stream.
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    e = cudaMemsetAsync(counters, 0, static_cast<size_t>(plan->d.n_head + plan->d.n_head_kv) * sizeof(uint32_t), s);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the library's FusedQkvNorm counters");
+    return run_qknorm(plan, x, ws, bs, q_norm_w, k_norm_w, eps, d_pos, q, k, v, kv_k, kv_v, counters, false, s);
+}
+
 extern "C" qkv_status qkv_decode_step_mixed(const qkv_plan* plan, const float* x, const void* wq,
                                             const void* wk, const void* wv, const float* bias_q,
                                             const float* bias_k, const float* bias_v,

@@ -54,6 +54,11 @@ cudaError_t launch_ffn(const DecodeParams& p, int w_dtype, bool pdl, cudaStream_
 // zeroed workspace of nh + nkv counters, left zeroed.  Rows must be 16-byte aligned.
 // Returns cudaErrorNotSupported when no ring shape fits the hidden size.
 cudaError_t launch_qknorm(const DecodeParams& p, int w_dtype, bool pdl, cudaStream_t stream);
+// The library's own FusedQkvNorm counters (a fixed device array of kQknormStaticHeads
+// entries): their device address on the current device, looked up on first use there.
+constexpr int kQknormStaticHeads = 1024;
+constexpr int kQknormMaxDevices = 64;
+cudaError_t qknorm_static_workspace(unsigned int** out);
 
 // prefill_tcgen05.cu
 struct PrefillParams {
