@@ -78,13 +78,12 @@ __device__ __forceinline__ void flag_bad_pos(int pos) {
 
 __device__ __forceinline__ void flag_timeout() { atomicOr(&g_qkv_status[0], kFlagTimeout); }
 
-// q (sec 0) or k (sec 1) pair: bias (b0, b1 already loaded), rotate, write back;
-// k also goes to the cache.
-// q/k pair (j, j2) after the bias: rotate, write back, store k rows to the cache.
-__device__ __forceinline__ void epi_qk_rot(const DecodeParams& p, int sec, int j, int j2, float x0, float x1,
-                                           int pos, float inv_freq, bool store) {
+// q/k pair (j, j2) after the bias: rotate by the angle whose (cos, sin) is cs, write
+// back, store k rows to the cache.
+__device__ __forceinline__ void epi_qk_rot_cs(const DecodeParams& p, int sec, int j, int j2, float x0, float x1,
+                                              int pos, float2 cs, bool store) {
     float r0, r1;
-    rope_rotate(x0, x1, rope_theta(pos, inv_freq), r0, r1);
+    rope_rotate_cs(x0, x1, cs, r0, r1);
     float* o = p.out[sec];
     o[j] = r0;
     o[j2] = r1;
@@ -93,6 +92,12 @@ __device__ __forceinline__ void epi_qk_rot(const DecodeParams& p, int sec, int j
         kv_put(p.kv_k, p.kv_f16, row + j, r0);
         kv_put(p.kv_k, p.kv_f16, row + j2, r1);
     }
+}
+
+// The same with the angle of frequency inv_freq at pos.
+__device__ __forceinline__ void epi_qk_rot(const DecodeParams& p, int sec, int j, int j2, float x0, float x1,
+                                           int pos, float inv_freq, bool store) {
+    epi_qk_rot_cs(p, sec, j, j2, x0, x1, pos, rope_cos_sin(pos, inv_freq), store);
 }
 
 __device__ __forceinline__ void epi_qk_pair_b(const DecodeParams& p, int sec, int j, int j2, float y0, float y1,
@@ -566,7 +571,7 @@ __global__ void __launch_bounds__((kGroups * kGroupWarps + 1) * 32, 2)
                           uint32_t x_bytes, int skew) {
     constexpr int kConsumerWarps = kGroups * kGroupWarps;
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ float freq_s[QKV_MAX_HEAD_DIM / 2];
+    __shared__ float2 cs_s[QKV_MAX_HEAD_DIM / 2];  // (cos, sin) of each pair index at pos
     __shared__ float gpart[kGroups][kGroupWarps][2];
     float4* xs4 = reinterpret_cast<float4*>(smem);
     unsigned char* ring = smem + x_bytes;
@@ -624,14 +629,16 @@ __global__ void __launch_bounds__((kGroups * kGroupWarps + 1) * 32, 2)
     // ---- consumers ----
     prefetch_norm(p, threadIdx.x, kConsumerWarps * 32);
     griddep_wait();
+    const int pos = (MODE == kFused) ? *p.pos : 0;
     {
+        // Every head rotates pair d by the same angle: its (cos, sin) are computed once here.
         const int tid = threadIdx.x, nthr = kConsumerWarps * 32;
         stage_input<WT, true>(p, xs4, tid, nthr);
-        for (int i = tid; i < half; i += nthr) freq_s[i] = p.inv_freq[i];
+        if (MODE == kFused)
+            for (int i = tid; i < half; i += nthr) cs_s[i] = rope_cos_sin(pos, p.inv_freq[i]);
     }
     named_barrier_sync(1, kConsumerWarps * 32);
     const float inv = norm_inv(p, kConsumerWarps * 32);
-    const int pos = (MODE == kFused) ? *p.pos : 0;
     const bool store = pos_ok(pos, p.n_ctx);
     if (MODE == kFused && !store && blockIdx.x == 0 && threadIdx.x == 0) flag_bad_pos(pos);
 
@@ -687,7 +694,8 @@ __global__ void __launch_bounds__((kGroups * kGroupWarps + 1) * 32, 2)
                     p.out[t.sec][r0] = a0;
                     p.out[t.sec][r1] = a1;
                 } else if (t.sec < 2) {
-                    epi_qk_pair_b(p, t.sec, r0, r1, a0, a1, b0, b1, pos, freq_s[r0 % p.hd], store);
+                    epi_qk_rot_cs(p, t.sec, r0, r1, __fadd_rn(a0, b0), __fadd_rn(a1, b1), pos, cs_s[r0 % p.hd],
+                                  store);
                 } else {
                     epi_v_elem_b(p, r0, a0, b0, pos, store);
                     epi_v_elem_b(p, r1, a1, b1, pos, store);
@@ -743,7 +751,7 @@ __device__ __forceinline__ float swiglu(float g, float u) {
 // (z_d inv w_d, z_{d+hd/2} inv w_{d+hd/2}), rotated and stored as in the plain stage.
 // The values are read at L2 (ld.global.cg): other SMs wrote them.
 __device__ __forceinline__ void qknorm_finish_head(const DecodeParams& p, int hh, int pos, bool store,
-                                                   const float* freq_s, int lane) {
+                                                   const float2* cs_s, int lane) {
     const int hd = p.hd, half = hd >> 1;
     const int nhq = p.nqt / hd;
     const int sec = hh < nhq ? 0 : 1;
@@ -760,7 +768,7 @@ __device__ __forceinline__ void qknorm_finish_head(const DecodeParams& p, int hh
     for (int d = lane; d < half; d += 32) {
         const float n0 = __fmul_rn(__fmul_rn(__ldcg(z + d), inv), __ldg(w + d));
         const float n1 = __fmul_rn(__fmul_rn(__ldcg(z + d + half), inv), __ldg(w + d + half));
-        epi_qk_rot(p, sec, base + d, base + d + half, n0, n1, pos, freq_s[d], store);
+        epi_qk_rot_cs(p, sec, base + d, base + d + half, n0, n1, pos, cs_s[d], store);
     }
 }
 
@@ -782,7 +790,7 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
     static_assert(kBlkPairs >= 1 && kBlkPairs <= 8, "rows per block");
     static_assert(kGroupWarps == 1, "one warp per consumer group");
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ float freq_s[QKV_MAX_HEAD_DIM / 2];
+    __shared__ float2 cs_s[QKV_MAX_HEAD_DIM / 2];  // (cos, sin) of each pair index at pos
     float4* xs4 = reinterpret_cast<float4*>(smem);
     unsigned char* ring = smem + x_bytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(ring + static_cast<size_t>(stages) * stage_bytes);
@@ -852,15 +860,16 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
     }
     prefetch_norm(p, threadIdx.x, kGroups * 32);
     griddep_wait();
+    const int pos = (MODE == kFused && EPI != kEpiSwiglu) ? *p.pos : 0;
     {
+        // Every head rotates pair d by the same angle: its (cos, sin) are computed once here.
         const int tid = threadIdx.x, nthr = kGroups * 32;
         stage_input<WT, true>(p, xs4, tid, nthr);
-        if (EPI != kEpiSwiglu)
-            for (int i = tid; i < (p.hd >> 1); i += nthr) freq_s[i] = p.inv_freq[i];
+        if (MODE == kFused && EPI != kEpiSwiglu)
+            for (int i = tid; i < (p.hd >> 1); i += nthr) cs_s[i] = rope_cos_sin(pos, p.inv_freq[i]);
     }
     named_barrier_sync(1, kGroups * 32);
     const float inv = norm_inv(p, kGroups * 32);
-    const int pos = (MODE == kFused && EPI != kEpiSwiglu) ? *p.pos : 0;
     const bool store = pos_ok(pos, p.n_ctx);
     if (MODE == kFused && EPI != kEpiSwiglu && !store && blockIdx.x == 0 && threadIdx.x == 0) flag_bad_pos(pos);
 
@@ -935,7 +944,7 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
                 // the partner block is complete: rotate the unit's pair lane
                 const float o = static_cast<volatile float*>(res)[e + (blk ? -kBlkPairs : kBlkPairs)];
                 const int r0 = t.r + lane;
-                epi_qk_rot(p, t.sec, r0, r0 + t.off, blk ? o : yb, blk ? yb : o, pos, freq_s[r0 % p.hd], store);
+                epi_qk_rot_cs(p, t.sec, r0, r0 + t.off, blk ? o : yb, blk ? yb : o, pos, cs_s[r0 % p.hd], store);
             }
         }
     }
@@ -959,7 +968,7 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
                         __threadfence();      // the other CTAs' values of head hh after their counts
                     }
                 }
-                if (__shfl_sync(0xffffffffu, last, 0)) qknorm_finish_head(p, hh, pos, store, freq_s, lane);
+                if (__shfl_sync(0xffffffffu, last, 0)) qknorm_finish_head(p, hh, pos, store, cs_s, lane);
             }
         }
     }

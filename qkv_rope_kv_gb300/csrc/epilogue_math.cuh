@@ -17,13 +17,25 @@ __device__ __forceinline__ float rope_theta(int pos, float inv_freq) {
     return __fmul_rn(__int2float_rn(pos), inv_freq);
 }
 
-// Neox rotation of the pair (x0, x1) = (element d, element d + hd/2):
-// (x0 cos - x1 sin, x0 sin + x1 cos).
+// (cos, sin) of the angle of pair index d at position pos: a kernel may compute them
+// once per pair index and reuse them for every head.
+__device__ __forceinline__ float2 rope_cos_sin(int pos, float inv_freq) {
+    float s, c;
+    sincosf(rope_theta(pos, inv_freq), &s, &c);
+    return make_float2(c, s);
+}
+
+// Neox rotation of the pair (x0, x1) = (element d, element d + hd/2) by the angle with
+// cos cs.x and sin cs.y: (x0 cos - x1 sin, x0 sin + x1 cos).
+__device__ __forceinline__ void rope_rotate_cs(float x0, float x1, float2 cs, float& r0, float& r1) {
+    r0 = __fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y));
+    r1 = __fadd_rn(__fmul_rn(x0, cs.y), __fmul_rn(x1, cs.x));
+}
+
 __device__ __forceinline__ void rope_rotate(float x0, float x1, float theta, float& r0, float& r1) {
     float s, c;
     sincosf(theta, &s, &c);
-    r0 = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, s));
-    r1 = __fadd_rn(__fmul_rn(x0, s), __fmul_rn(x1, c));
+    rope_rotate_cs(x0, x1, make_float2(c, s), r0, r1);
 }
 
 // Cache element store at flat index pos * nkt + j (f32, or f16 round-to-nearest-even).
