@@ -464,6 +464,7 @@ struct Unit {
     int r;    // first row of block A (section-local)
     int n;    // rows per block
     int off;  // block B starts at row r + off
+    int d;    // q / k: pair index of row r within its head (r mod hd); v: 0
 };
 
 template <int P = kPairs>
@@ -480,11 +481,13 @@ __device__ __forceinline__ Unit unit_info(int u, int nqt, int nkt, int hd) {
         t.n = min(P, half - d0);
         t.r = h * hd + d0;
         t.off = half;
+        t.d = d0;
     } else {
         t.sec = 2;
         t.r = (u - uq - uk) * 2 * P;
         t.n = min(P, (nkt - t.r) >> 1);
         t.off = t.n;
+        t.d = 0;
     }
     return t;
 }
@@ -500,10 +503,12 @@ __host__ __device__ __forceinline__ int unit_count(int nqt, int nkt, int hd) {
 // values (heads, units per head) in every item: +1 % on the 14B graph.  (In the pair
 // ring the table measured 0.6-2 % slower, so it decodes per item.)
 constexpr int kUnitTable = 64;
-__device__ __forceinline__ int4 pack_unit(const Unit& t) { return make_int4(t.sec, t.r, t.n, t.off); }
+// (sec, d) share the first word: sec in bits 0-1, d above.
+__device__ __forceinline__ int4 pack_unit(const Unit& t) { return make_int4(t.sec | (t.d << 2), t.r, t.n, t.off); }
 __device__ __forceinline__ Unit unpack_unit(int4 v) {
     Unit t;
-    t.sec = v.x;
+    t.sec = v.x & 3;
+    t.d = v.x >> 2;
     t.r = v.y;
     t.n = v.z;
     t.off = v.w;
@@ -709,7 +714,7 @@ __global__ void __launch_bounds__((kGroups * kGroupWarps + 1) * 32, 2)
                     p.out[t.sec][r0] = a0;
                     p.out[t.sec][r1] = a1;
                 } else if (t.sec < 2) {
-                    epi_qk_rot_cs(p, t.sec, r0, r1, __fadd_rn(a0, b0), __fadd_rn(a1, b1), pos, cs_s[r0 % p.hd],
+                    epi_qk_rot_cs(p, t.sec, r0, r1, __fadd_rn(a0, b0), __fadd_rn(a1, b1), pos, cs_s[t.d + j],
                                   store);
                 } else {
                     epi_v_elem_b(p, r0, a0, b0, pos, store);
@@ -747,6 +752,7 @@ __device__ __forceinline__ Unit blk_unit(int u, const DecodeParams& p) {
     } else {
         Unit t;
         t.sec = 0;
+        t.d = 0;
         t.r = u * kBlkPairs;
         t.n = min(kBlkPairs, p.nf - t.r);
         t.off = p.nf;
@@ -962,7 +968,7 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
                 // the partner block is complete: rotate the unit's pair lane
                 const float o = static_cast<volatile float*>(res)[e + (blk ? -kBlkPairs : kBlkPairs)];
                 const int r0 = t.r + lane;
-                epi_qk_rot_cs(p, t.sec, r0, r0 + t.off, blk ? o : yb, blk ? yb : o, pos, cs_s[r0 % p.hd], store);
+                epi_qk_rot_cs(p, t.sec, r0, r0 + t.off, blk ? o : yb, blk ? yb : o, pos, cs_s[t.d + lane], store);
             }
         }
     }
