@@ -72,8 +72,15 @@ def measured_peak():
 
 
 def source_hash(rel_path: str) -> str:
-    with open(os.path.join(ROOT, rel_path), "rb") as fh:
-        return hashlib.sha256(fh.read()).hexdigest()
+    """SHA-256 of a kernel source with its comments and blank lines removed: a traffic
+    capture stays valid across comment edits, and only across those."""
+    import re
+    with open(os.path.join(ROOT, rel_path), encoding="utf-8") as fh:
+        text = fh.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    lines = [ln.rstrip() for ln in text.splitlines() if ln.strip()]
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()
 
 
 def traffic_per_launch(workload_name: str):

@@ -1,30 +1,40 @@
 // Decode (nt == 1) kernels of the attention-input stage on sm_103a.
 //
-//   qkv_decode_kernel   the projection y = W x over the q | k | v rows, one
-//                       neox pair of rows per warp, with the epilogue (bias,
-//                       RoPE, KV-cache store) in the warp's tail — one launch
-//                       per layer for both layer classes.  The same kernel in
-//                       projection-only mode writes the raw y.
-//   qkv_epilogue_kernel the epilogue alone over the flat index
-//                       nqt/2 + nkt/2 + nkt ("73 · D3-8 — G4 FusedQKV ported to
-//                       CUDA", §3.2 Excerpts A and B).
-//   qkv_chain_*         the seven-launch chain the fusion replaces (same page,
-//                       §2): kept as bitwise comparators.
+//   qkv_decode_blk_kernel  block ring, rows of >= 8 KB (the 14B shape): persistent
+//                          CTAs, one per SM; a producer lane streams blocks of
+//                          two adjacent rows into a shared-memory ring with
+//                          cp.async.bulk, five one-warp consumer groups reduce
+//                          them and finish each unit's neox pairs (bias, RoPE,
+//                          KV-cache store).  The same ring runs the FusedFFN
+//                          (silu(gate) * up) and the FusedQkvNorm stage.
+//   qkv_decode_tma_kernel  pair ring, shorter 16-byte aligned rows (7B, 0.5B):
+//                          two CTAs per SM, one neox pair (two copies) per stage.
+//   qkv_decode_kernel      register streaming, one row pair per warp with
+//                          16-byte non-allocating loads: rows that are not
+//                          16-byte aligned or too long to stage.
+//   qkv_epilogue_kernel    the epilogue alone over the flat index
+//                          nqt/2 + nkt/2 + nkt ("73 · D3-8 — G4 FusedQKV ported
+//                          to CUDA", §3.2 Excerpts A and B).
+//   qkv_chain_*            the seven-launch chain the fusion replaces (same page,
+//                          §2): kept as bitwise comparators.
+// Every kernel except the comparators writes the fused result in one launch per
+// layer, for both layer classes; in projection-only mode the rings write the raw y.
 //
-// All three epilogue forms call the same device functions below, in the same
-// order of f32 operations (explicit _rn intrinsics, no contraction), so their
-// results agree bit for bit — the page's gate for the fusion (§2, "The
-// fusion's bitwise legitimacy").
+// All epilogue forms call the same device functions below, in the same order of
+// f32 operations (explicit _rn intrinsics, no contraction), so their results
+// agree bit for bit — the page's gate for the fusion (§2, "The fusion's bitwise
+// legitimacy").  The rings take each pair's (cos, sin) from a table the CTA fills
+// once per launch with the same sincosf of the same f32 angle.
 //
 // Projection design (HBM-bound: ~1 flop per weight byte against a ridge of
-// ~270 flop/B): every weight byte is read once with 16-byte non-allocating
-// loads, each lane streams a strided share of the two rows of its pair, x is
-// staged once per CTA in shared memory, and the two dot products are reduced
-// with a xor-shuffle butterfly (identical result in every lane).  A pair of
-// rows (j, j + hd/2) of one head lands in one warp, so RoPE needs no exchange
-// between warps.  Each row is reduced by the same code whatever class the
-// layer has, so a concat layer and the same rows split into wq / wk / wv give
-// identical bits (same page, §2, "Why the concat matmul is bitwise").
+// ~270 flop/B): every weight byte is read from HBM once, x is staged once per CTA
+// in shared memory, each lane takes a strided share of a row's 16-byte chunks, and
+// the dot products are reduced with a xor-shuffle butterfly (identical result in
+// every lane).  Both rows of a neox pair (j, j + hd/2) of one head are finished in
+// one place, so RoPE needs no exchange between CTAs.  Each row is reduced by the
+// same code whatever class the layer has, so a concat layer and the same rows split
+// into wq / wk / wv give identical bits (same page, §2, "Why the concat matmul is
+// bitwise").
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
