@@ -28,3 +28,18 @@ def test_bench_help_lists_workloads():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--help"], capture_output=True, text=True,
                        timeout=120, cwd=ROOT)
     assert r.returncode == 0 and "qwen2.5-14b-48layer-mixed" in r.stdout
+
+
+def test_traffic_record_keys_ignore_comments(tmp_path, monkeypatch):
+    """A DRAM-traffic capture stays valid across comment edits of its kernel source and is
+    voided by a code edit."""
+    sys.path.insert(0, ROOT)
+    import bench
+    src = tmp_path / "k.cu"
+    src.write_text("// header\nint f(int a) {  // trailing\n  /* block\n comment */ return a + 1;\n}\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.source_hash("k.cu")
+    src.write_text("// header\nint f(int a) {  // trailing\n  /* other\n words */ return a + 1;\n}\n")
+    assert bench.source_hash("k.cu") == h0
+    src.write_text("// header\nint f(int a) {  // trailing\n  /* block\n comment */ return a + 2;\n}\n")
+    assert bench.source_hash("k.cu") != h0
