@@ -460,6 +460,13 @@ constexpr int kGroupWarps = QKV_DECODE_GROUP_WARPS;   // G: warps per group
 constexpr int kGroupsLarge = QKV_DECODE_LARGE_GROUPS;
 constexpr int kGroupsSmall = QKV_DECODE_SMALL_GROUPS;
 constexpr size_t kSmallRowBytes = 8192;
+// Rows under 4 KB (the 0.5B shape's 3.5 KB f32 rows) run the pair ring three CTAs per SM
+// with two groups each: more, smaller CTAs, so a layer's CTAs start while the previous
+// layer's are still finishing (0.5B sweep +13 %; the 7 KB rows of the 7B shape lose with it).
+constexpr int kGroupsTiny = 2;
+constexpr int kTinyCtas = 3;
+constexpr int kTinySmemKb = 72;
+constexpr size_t kTinyRowBytes = 4096;
 
 #ifndef QKV_DECODE_PAIRS
 #define QKV_DECODE_PAIRS 1
@@ -1224,6 +1231,9 @@ cudaError_t launch_decode_t(const DecodeParams& p, bool pdl, cudaStream_t stream
             if (launched || e != cudaSuccess) return e;
             const RingShape r = ring_shape<WT>(p, kGroupsLarge, QKV_DECODE_LARGE_CTAS, QKV_DECODE_LARGE_SMEM_KB);
             if (r.stages > 0) return launch_decode_tma<WT, MODE, kGroupsLarge>(p, r, pdl, stream);
+        } else if (row < kTinyRowBytes) {
+            const RingShape r = ring_shape<WT>(p, kGroupsTiny, kTinyCtas, kTinySmemKb);
+            if (r.stages > 0) return launch_decode_tma<WT, MODE, kGroupsTiny>(p, r, pdl, stream);
         } else {
             const RingShape r = ring_shape<WT>(p, kGroupsSmall, QKV_DECODE_SMALL_CTAS, QKV_DECODE_SMALL_SMEM_KB);
             if (r.stages > 0) return launch_decode_tma<WT, MODE, kGroupsSmall>(p, r, pdl, stream);
