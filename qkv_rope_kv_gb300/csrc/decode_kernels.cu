@@ -462,7 +462,7 @@ constexpr int kGroupsSmall = QKV_DECODE_SMALL_GROUPS;
 constexpr size_t kSmallRowBytes = 8192;
 // Rows under 4 KB (the 0.5B shape's 3.5 KB f32 rows) run the pair ring three CTAs per SM
 // with two groups each: more, smaller CTAs, so a layer's CTAs start while the previous
-// layer's are still finishing (0.5B sweep +13 %; the 7 KB rows of the 7B shape lose with it).
+// layer's are still finishing (0.5B sweep +12 %; the 7 KB rows of the 7B shape lose with it).
 constexpr int kGroupsTiny = 2;
 constexpr int kTinyCtas = 3;
 constexpr int kTinySmemKb = 72;
