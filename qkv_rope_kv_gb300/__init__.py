@@ -246,7 +246,7 @@ def qkv_epilogue(plan: Plan, q, k, v, bias_q, bias_k, bias_v, d_pos, kv_k, kv_v,
 
 
 def qkv_chain_add_bias(y, b, n: int, stream=None):
-    _check(_lib.qkv_chain_add_bias(_ptr(y), _ptr(b), n, _stream(stream)))
+    _check(load().qkv_chain_add_bias(_ptr(y), _ptr(b), n, _stream(stream)))
 
 
 def qkv_chain_rope(plan: Plan, y, n_heads: int, d_pos, stream=None):
@@ -396,7 +396,7 @@ def qkv_prefill_graph_create(plans, layers, nt: int, stream) -> ModelGraph:
 
 def qkv_ffn_step(hidden: int, n_ff: int, w_dtype: int, x, w_gate_up, out, stream=None):
     """out[i] = silu(g_i) * u_i over the concat gate|up weight (device tensors)."""
-    _check(_lib.qkv_ffn_step(hidden, n_ff, w_dtype, _ptr(x), _ptr(w_gate_up), _ptr(out), _stream(stream)))
+    _check(load().qkv_ffn_step(hidden, n_ff, w_dtype, _ptr(x), _ptr(w_gate_up), _ptr(out), _stream(stream)))
 
 
 def qkv_ffn_graph_create(hidden: int, n_ff: int, w_dtype: int, layers, stream) -> ModelGraph:
@@ -407,7 +407,7 @@ def qkv_ffn_graph_create(hidden: int, n_ff: int, w_dtype: int, layers, stream) -
         for name, _ in qkv_ffn_layer._fields_:
             setattr(arr[i], name, _ptr(L.get(name)))
     h = ctypes.c_void_p()
-    _check(_lib.qkv_ffn_graph_create(hidden, n_ff, w_dtype, n, arr, _stream(stream), ctypes.byref(h)))
+    _check(load().qkv_ffn_graph_create(hidden, n_ff, w_dtype, n, arr, _stream(stream), ctypes.byref(h)))
     return ModelGraph(h.value, (layers,))
 
 
@@ -417,7 +417,7 @@ def qkv_check_device_error(stream=None, raise_on_flag: bool = False):
     """Return (flags, bad_pos) and clear the device status word."""
     flags = ctypes.c_uint32()
     bad = ctypes.c_int32()
-    st = _lib.qkv_check_device_error(_stream(stream), ctypes.byref(flags), ctypes.byref(bad))
+    st = load().qkv_check_device_error(_stream(stream), ctypes.byref(flags), ctypes.byref(bad))
     if st not in (QKV_OK, QKV_ERR_DEVICE_FLAG) or (raise_on_flag and st != QKV_OK):
         _check(st)
     return flags.value, bad.value

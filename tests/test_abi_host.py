@@ -2,6 +2,7 @@
 point include/qkv.h declares, validates arguments before touching CUDA, and its
 size arithmetic matches the numbers printed on the pages."""
 import ctypes
+import os
 
 import numpy as np
 import pytest
@@ -232,3 +233,22 @@ def test_qknorm_guards(lib):
         q.QKV_ERR_INVALID_ARG
     assert g(plans, 0, layers, norms, norms, ctypes.c_float(1e-6), fake, fake, fake, ctypes.byref(h)) == \
         q.QKV_ERR_INVALID_ARG
+
+
+def test_plan_free_entry_points_load_the_library():
+    """Entry points that take no plan load libqkv.so themselves: in a fresh interpreter,
+    null arguments come back as the library's own INVALID_ARG status."""
+    import subprocess
+    import sys
+    code = ("import qkv_rope_kv_gb300 as Q\n"
+            "for f, a in ((Q.qkv_chain_add_bias, (None, None, 1)),\n"
+            "             (Q.qkv_ffn_step, (8, 4, Q.QKV_F32, None, None, None))):\n"
+            "    try:\n"
+            "        f(*a, stream=0)\n"
+            "    except Q.QkvError as e:\n"
+            "        assert e.status == Q.QKV_ERR_INVALID_ARG, e\n"
+            "    else:\n"
+            "        raise SystemExit('no error for null pointers')\n")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300,
+                       cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    assert r.returncode == 0, r.stdout + r.stderr
