@@ -252,3 +252,45 @@ def test_plan_free_entry_points_load_the_library():
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300,
                        cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
     assert r.returncode == 0, r.stdout + r.stderr
+
+
+def _c_kind(decl: str) -> str:
+    """Category of a C parameter or return type (without its name) as it crosses the ABI."""
+    if "*" in decl:
+        return "ptr"
+    base = decl.replace("const", "").split()[0]
+    return {"float": "f32", "int32_t": "i32", "int": "i32", "qkv_status": "i32", "int64_t": "i64",
+            "size_t": "size", "void": "void", "uint32_t": "u32"}[base]
+
+
+def _ctypes_kind(t) -> str:
+    if t is None:
+        return "void"
+    if t in (ctypes.c_void_p, ctypes.c_char_p) or issubclass(t, ctypes._Pointer):
+        return "ptr"
+    return {ctypes.c_float: "f32", ctypes.c_int32: "i32", ctypes.c_int64: "i64",
+            ctypes.c_size_t: "size", ctypes.c_uint32: "u32"}[t]
+
+
+def _signature_mismatches(lib):
+    import re
+    text = re.sub(r"/\*.*?\*/", "", open(q.HEADER).read(), flags=re.S)
+    protos = re.findall(r"\n([A-Za-z_][\w\s\*]*?)\b((?:qkv|kv)_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", text)
+    assert sorted(name for _, name, _ in protos) == q.header_entry_points()
+    bad = []
+    for ret, name, args in protos:
+        # every parameter in the header is named: its type is all but the last token
+        params = [] if args.strip() in ("", "void") else [a.strip().rsplit(None, 1)[0] for a in args.split(",")]
+        want = ([_c_kind(t) for t in params], _c_kind(ret))
+        fn = getattr(lib, name)
+        got = ([_ctypes_kind(t) for t in (fn.argtypes or [])], _ctypes_kind(fn.restype))
+        if got != want:
+            bad.append((name, got, want))
+    return bad
+
+
+def test_binding_signatures_match_header(lib):
+    """Every prototype in include/qkv.h and the ctypes declaration of the same name agree on
+    the number of parameters, each one's kind (pointer, f32, 32/64-bit integer, size_t) and
+    the return kind: a drifted declaration would pass garbage without an error."""
+    assert _signature_mismatches(lib) == []
