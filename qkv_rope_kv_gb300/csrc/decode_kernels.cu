@@ -8,7 +8,9 @@
 //                          KV-cache store).  The same ring runs the FusedFFN
 //                          (silu(gate) * up) and the FusedQkvNorm stage.
 //   qkv_decode_tma_kernel  pair ring, shorter 16-byte aligned rows (7B, 0.5B):
-//                          two CTAs per SM, one neox pair (two copies) per stage.
+//                          one neox pair (two copies) per stage; two CTAs per
+//                          SM with three consumer groups (rows of 4-8 KB), or
+//                          three with two groups (rows under 4 KB).
 //   qkv_decode_kernel      register streaming, one row pair per warp with
 //                          16-byte non-allocating loads: rows that are not
 //                          16-byte aligned or too long to stage.
