@@ -72,6 +72,12 @@ MUTANTS = {
                                 "oracle_rope_pair(n0, n1, 0.0f, 0.0f, 0, f, &out[d], &out[d + half]);"),
     "qknorm_k_not_stored": ("for (int i = 0; i < hd; ++i) kv_put(kv_k, kv_is_f16, row + (size_t)(h * hd + i), k_out[h * hd + i]);",
                             "for (int i = 0; i + 1 < hd; ++i) kv_put(kv_k, kv_is_f16, row + (size_t)(h * hd + i), k_out[h * hd + i]);"),
+    "prefill_every_token_reads_x0": ("x_scratch[c] = (float)oracle_bf16_value(X[(int64_t)t * hidden + c]);",
+                                     "x_scratch[c] = (float)oracle_bf16_value(X[c]);"),
+    "prefill_first_position_only": ("freq_scale, positions[t], n_ctx, kv_is_f16, y_scratch, yt,",
+                                    "freq_scale, positions[0], n_ctx, kv_is_f16, y_scratch, yt,"),
+    "mixed_wk_wv_swapped": ("oracle_matvec(Wk, w_is_bf16, x, nkt, hidden, y_scratch + nqt);",
+                            "oracle_matvec(Wv, w_is_bf16, x, nkt, hidden, y_scratch + nqt);"),
     "ffn_drops_last_column": ("for (int64_t c = 0; c < H; ++c) {\n                g += (double)rg[c]",
                               "for (int64_t c = 0; c + 1 < H; ++c) {\n                g += (double)rg[c]"),
 }
