@@ -72,6 +72,11 @@ MUTANTS = {
                                 "oracle_rope_pair(n0, n1, 0.0f, 0.0f, 0, f, &out[d], &out[d + half]);"),
     "qknorm_k_not_stored": ("for (int i = 0; i < hd; ++i) kv_put(kv_k, kv_is_f16, row + (size_t)(h * hd + i), k_out[h * hd + i]);",
                             "for (int i = 0; i + 1 < hd; ++i) kv_put(kv_k, kv_is_f16, row + (size_t)(h * hd + i), k_out[h * hd + i]);"),
+    "freq_scale_ignored": ("const long double v = (long double)freq_scale * powl((long double)base, ex);",
+                           "const long double v = powl((long double)base, ex);"),
+    "q_freq_index_shifted": ("const float f = oracle_inv_freq(d, hd, base, freq_scale);\n            oracle_rope_pair(yq[j]",
+                             "const float f = oracle_inv_freq(d + 1, hd, base, freq_scale);\n            oracle_rope_pair(yq[j]"),
+    "out_of_range_reports_ok": ("return store ? ORACLE_OK : ORACLE_POS_RANGE;", "return ORACLE_OK;"),
     "prefill_every_token_reads_x0": ("x_scratch[c] = (float)oracle_bf16_value(X[(int64_t)t * hidden + c]);",
                                      "x_scratch[c] = (float)oracle_bf16_value(X[c]);"),
     "prefill_first_position_only": ("freq_scale, positions[t], n_ctx, kv_is_f16, y_scratch, yt,",
