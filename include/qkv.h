@@ -341,8 +341,10 @@ qkv_status qkv_decode_step_qknorm(const qkv_plan* plan, const float* x, const vo
  * by the library.  The pages have no counterpart of this entry point.
  *   - At most 1024 q + kv heads (nh + nkv); larger plans get INVALID_ARG.
  *   - The first call on a device looks up the array's device address there
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture on the device.
+ *     (cudaGetSymbolAddress, with that device current) and keeps it for the
+ *     device's current context; make that first call before any stream
+ *     capture on the device.  After cudaDeviceReset the next call runs in a
+ *     new context and looks the address up again (the same rule applies to it).
  *   - Every call clears the counters it uses (an asynchronous memset on
  *     `stream`) and shares the one array with every other call on the device:
  *     calls that may overlap on the GPU (different streams, or graph replays

@@ -188,7 +188,7 @@ class Oracle:
         W = np.ascontiguousarray(W)
         assert W.shape[0] == R
         assert len(q_norm_w) == hd and len(k_norm_w) == hd
-        y = np.empty(R, np.float64)
+        y = np.full(R, np.nan)  # a row the oracle fails to compute shows up as NaN
         q = np.empty(nqt, np.float32)
         k = np.empty(nkt, np.float32)
         v = np.empty(nkt, np.float32)
@@ -209,7 +209,7 @@ class Oracle:
         W = np.ascontiguousarray(W)
         assert W.shape[0] == R
         H = W.shape[1]
-        y = np.empty(R, np.float64)
+        y = np.full(R, np.nan)  # a row the oracle fails to compute shows up as NaN
         q = np.empty(nqt, np.float32)
         k = np.empty(nkt, np.float32)
         v = np.empty(nkt, np.float32)
@@ -226,7 +226,7 @@ class Oracle:
         Wq, Wk, Wv = (np.ascontiguousarray(a) for a in (Wq, Wk, Wv))
         assert Wq.dtype == Wk.dtype == Wv.dtype
         H = Wq.shape[1]
-        y = np.empty(nqt + 2 * nkt, np.float64)
+        y = np.full(nqt + 2 * nkt, np.nan)  # a row the oracle fails to compute shows up as NaN
         q = np.empty(nqt, np.float32)
         k = np.empty(nkt, np.float32)
         v = np.empty(nkt, np.float32)
@@ -246,7 +246,7 @@ class Oracle:
         nt, H = X_bf16.shape
         positions = np.ascontiguousarray(positions, np.int32)
         xs = np.empty(H, np.float32)
-        ys = np.empty(R, np.float64)
+        ys = np.full(R, np.nan)
         Y = np.empty((nt, R), np.float32)
         n_ctx, f16 = _kv_meta(kv_k, kv_v, nkt)
         st = self.lib.oracle_qkv_prefill(_p(X_bf16), nt, _p(W), int(W.dtype == np.uint16),

@@ -20,6 +20,8 @@ import threading
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libqkv.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "qkv.h")
+# every header of the C ABI: the stage (qkv.h) and the test hook of its failure path (qkv_test.h)
+HEADERS = (HEADER, os.path.join(os.path.dirname(_HERE), "include", "qkv_test.h"))
 
 # ---- constants mirrored from include/qkv.h ----
 QKV_OK, QKV_ERR_INVALID_ARG, QKV_ERR_UNSUPPORTED, QKV_ERR_POS_RANGE, QKV_ERR_CUDA, \
@@ -134,6 +136,7 @@ def _declare(lib):
         "qkv_model_graph_create_qknorm": ([vp, i32, vp, vp, vp, ctypes.c_float, vp, vp, vp, ctypes.POINTER(vp)], st),
         "qkv_model_graph_destroy": ([vp], None),
         "qkv_check_device_error": ([vp, ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(i32)], st),
+        "qkv_test_decode_wait_timeout": ([vp] * 10 + [ctypes.c_uint32, vp], st),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -141,9 +144,9 @@ def _declare(lib):
         fn.restype = res
 
 
-def header_entry_points(path: str = HEADER) -> list[str]:
-    """Names of the functions include/qkv.h declares."""
-    text = open(path).read()
+def header_entry_points(paths=HEADERS) -> list[str]:
+    """Names of the functions the headers of include/ declare."""
+    text = "".join(open(p).read() for p in ([paths] if isinstance(paths, str) else paths))
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b((?:qkv|kv)_[a-z0-9_]+)\s*\(", text)))
 
@@ -217,6 +220,15 @@ def qkv_plan_create(hidden: int, n_head: int, n_head_kv: int, head_dim: int, the
 def qkv_decode_step(plan: Plan, x, w, bias, d_pos, q, k, v, kv_k, kv_v, stream=None):
     _check(_lib.qkv_decode_step(plan.handle, _ptr(x), _ptr(w), _ptr(bias), _ptr(d_pos), _ptr(q),
                                 _ptr(k), _ptr(v), _ptr(kv_k), _ptr(kv_v), _stream(stream)))
+
+
+def qkv_test_decode_wait_timeout(plan: Plan, x, w, bias, d_pos, q, k, v, kv_k, kv_v, wait_limit_us: int = 200,
+                                 stream=None):
+    """Test hook (include/qkv_test.h): qkv_decode_step with each CTA's last weight copy withheld
+    and every wait limited to wait_limit_us, so the device status flag 2 gets set."""
+    _check(_lib.qkv_test_decode_wait_timeout(plan.handle, _ptr(x), _ptr(w), _ptr(bias), _ptr(d_pos), _ptr(q),
+                                             _ptr(k), _ptr(v), _ptr(kv_k), _ptr(kv_v), int(wait_limit_us),
+                                             _stream(stream)))
 
 
 def qkv_decode_step_rmsnorm(plan: Plan, h, norm_w, norm_eps: float, w, bias, d_pos, q, k, v, kv_k, kv_v,

@@ -36,7 +36,7 @@ def _sources():
 
 def _deps():
     return _sources() + sorted(glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh"))) + \
-        [os.path.join(INCLUDE, "qkv.h")]
+        sorted(glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
 def up_to_date() -> bool:

@@ -37,6 +37,7 @@
 // same code whatever class the layer has, so a concat layer and the same rows split
 // into wq / wk / wv give identical bits (same page, §2, "Why the concat matmul is
 // bitwise").
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -89,6 +90,11 @@ __device__ __forceinline__ void flag_bad_pos(int pos) {
 }
 
 __device__ __forceinline__ void flag_timeout() { atomicOr(&g_qkv_status[0], kFlagTimeout); }
+
+// Limit of every bounded wait of a launch: the default, unless a test shortened it.
+__device__ __forceinline__ uint64_t wait_limit(const DecodeParams& p) {
+    return p.wait_limit_ns ? p.wait_limit_ns : kWaitTimeoutNs;
+}
 
 // q/k pair (j, j2) after the bias: rotate by the angle whose (cos, sin) is cs, write
 // back, store k rows to the cache.
@@ -641,10 +647,12 @@ __global__ void __launch_bounds__((kGroups * kGroupWarps + 1) * 32, 2)
         // ---- producer: one lane issues all bulk copies of this CTA ----
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
+            const uint64_t limit = wait_limit(p);
+            const int n_issue = p.withhold_last_copy ? n - 1 : n;
             int issued = 0;
-            for (int i = 0; i < n; ++i) {
+            for (int i = 0; i < n_issue; ++i) {
                 const int s = i % stages;
-                if (i >= stages && !mbar_wait_bounded(&empty[s], ((i / stages) - 1) & 1)) {
+                if (i >= stages && !mbar_wait_bounded(&empty[s], ((i / stages) - 1) & 1, limit)) {
                     flag_timeout();
                     break;
                 }
@@ -660,12 +668,13 @@ __global__ void __launch_bounds__((kGroups * kGroupWarps + 1) * 32, 2)
             // Drain: no copy may still be landing in shared memory when the CTA exits.
             const int first = issued > stages ? issued - stages : 0;
             for (int i = first; i < issued; ++i)
-                if (!mbar_wait_bounded(&full[i % stages], (i / stages) & 1)) flag_timeout();
+                if (!mbar_wait_bounded(&full[i % stages], (i / stages) & 1, limit)) flag_timeout();
         }
         return;
     }
 
     // ---- consumers ----
+    const uint64_t limit = wait_limit(p);
     prefetch_norm(p, threadIdx.x, kConsumerWarps * 32);
     griddep_wait();
     const int pos = (MODE == kFused) ? *p.pos : 0;
@@ -685,7 +694,7 @@ __global__ void __launch_bounds__((kGroups * kGroupWarps + 1) * 32, 2)
     const int gt = gw * 32 + lane;  // thread index within the group
     for (int i = group; i < n; i += kGroups) {
         const int s = i % stages;
-        if (!mbar_wait_bounded(&full[s], (i / stages) & 1)) {
+        if (!mbar_wait_bounded(&full[s], (i / stages) & 1, limit)) {
             if (lane == 0) flag_timeout();
             break;
         }
@@ -864,10 +873,12 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
         // ---- producer: one lane issues all bulk copies of this CTA ----
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
+            const uint64_t limit = wait_limit(p);
+            const int n_issue = p.withhold_last_copy ? n - 1 : n;
             int issued = 0;
-            for (int i = 0; i < n; ++i) {
+            for (int i = 0; i < n_issue; ++i) {
                 const int st = i % stages;
-                if (i >= stages && !mbar_wait_bounded(&empty[st], ((i / stages) - 1) & 1)) {
+                if (i >= stages && !mbar_wait_bounded(&empty[st], ((i / stages) - 1) & 1, limit)) {
                     flag_timeout();
                     break;
                 }
@@ -883,12 +894,13 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
             // Drain: no copy may still be landing in shared memory when the CTA exits.
             const int first = issued > stages ? issued - stages : 0;
             for (int i = first; i < issued; ++i)
-                if (!mbar_wait_bounded(&full[i % stages], (i / stages) & 1)) flag_timeout();
+                if (!mbar_wait_bounded(&full[i % stages], (i / stages) & 1, limit)) flag_timeout();
         }
         return;
     }
 
     // ---- consumers ----
+    const uint64_t limit = wait_limit(p);
     // Biases are parameters, not outputs of an earlier kernel: stage this CTA's
     // share before the dependency wait, so no global load sits in the item loop.
     if (MODE == kFused && EPI != kEpiSwiglu) {
@@ -918,7 +930,7 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
 
     for (int i = warp; i < n; i += kGroups) {
         const int st = i % stages;
-        if (!mbar_wait_bounded(&full[st], (i / stages) & 1)) {
+        if (!mbar_wait_bounded(&full[st], (i / stages) & 1, limit)) {
             if (lane == 0) flag_timeout();
             break;
         }
@@ -1011,7 +1023,11 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
                         __threadfence();      // the other CTAs' values of head hh after their counts
                     }
                 }
-                if (__shfl_sync(0xffffffffu, last, 0)) qknorm_finish_head(p, hh, pos, store, cs_s, lane);
+                last = __shfl_sync(0xffffffffu, last, 0);
+                // A shuffle does not order memory: the barrier orders every lane's reads of
+                // the other CTAs' values after lane 0's acquiring fence.
+                __syncwarp();
+                if (last) qknorm_finish_head(p, hh, pos, store, cs_s, lane);
             }
         }
     }
@@ -1294,21 +1310,53 @@ cudaError_t launch_qknorm(const DecodeParams& p, int w_dtype, bool pdl, cudaStre
 // library, holding kQknormStaticHeads counters (4 KB).
 static __device__ __align__(256) unsigned int g_qknorm_static_counters[kQknormStaticHeads];
 
+// Id of the context current on this thread (0 when none is), through the driver entry
+// points the runtime exposes (no link against the driver library).
+static unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(f);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+        get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
 cudaError_t qknorm_static_workspace(unsigned int** out) {
     // Host code cannot use the array's name as a device address: look the address up
-    // once per device, with that device current, and reuse it.
+    // with the device current, once per device and context, and reuse it.  The context
+    // id keys the cache, so after cudaDeviceReset (which unloads the module; the next
+    // call runs in a new primary context) the address is looked up again.
     static std::mutex mu;
     static unsigned int* addr[kQknormMaxDevices] = {};
+    static unsigned long long ctx_of[kQknormMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kQknormMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
-    if (addr[dev] == nullptr) {
+    const unsigned long long ctx = current_context_id();
+    if (addr[dev] == nullptr || ctx == 0 || ctx != ctx_of[dev]) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_qknorm_static_counters);
         if (e != cudaSuccess) return e;
         addr[dev] = static_cast<unsigned int*>(p);
+        ctx_of[dev] = current_context_id();  // the lookup made the device's context current
     }
     *out = addr[dev];
     return cudaSuccess;

@@ -63,15 +63,16 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
-// Wait for the phase of parity `parity` to complete, giving up after
-// kWaitTimeoutNs (returns false; the caller flags the failure and stops).
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// Wait for the phase of parity `parity` to complete, giving up after limit_ns
+// (default kWaitTimeoutNs; returns false, and the caller flags the failure and stops).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitTimeoutNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 

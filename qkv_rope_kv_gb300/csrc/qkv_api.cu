@@ -14,6 +14,7 @@
 #include <vector>
 
 #include "qkv_internal.h"
+#include "qkv_test.h"
 
 namespace {
 
@@ -339,6 +340,45 @@ extern "C" qkv_status qkv_decode_step_qknorm_noalloc(const qkv_plan* plan, const
     e = cudaMemsetAsync(counters, 0, static_cast<size_t>(plan->d.n_head + plan->d.n_head_kv) * sizeof(uint32_t), s);
     if (e != cudaSuccess) return cuda_fail(e, "clearing the library's FusedQkvNorm counters");
     return run_qknorm(plan, x, ws, bs, q_norm_w, k_norm_w, eps, d_pos, q, k, v, kv_k, kv_v, counters, false, s);
+}
+
+// ------------------------------------------------------------------ test hook (include/qkv_test.h)
+
+extern "C" qkv_status qkv_test_decode_wait_timeout(const qkv_plan* plan, const float* x, const void* w,
+                                                   const float* bias, const int32_t* d_pos, float* q, float* k,
+                                                   float* v, void* kv_k, void* kv_v, uint32_t wait_limit_us,
+                                                   void* stream) {
+    REQUIRE(plan, "plan is null");
+    REQUIRE(plan->d.layer_class == QKV_CLASS_CONCAT, "qkv_test_decode_wait_timeout needs a concat-class plan");
+    REQUIRE(wait_limit_us >= 1 && wait_limit_us <= 1000, "wait_limit_us must be in [1, 1000]");
+    REQUIRE(w && bias, "w or bias is null");
+    const size_t es = elem_size(plan->d.w_dtype);
+    const char* wb = static_cast<const char*>(w);
+    const void* ws[3] = {wb, wb + plan->nqt * plan->d.hidden * es,
+                         wb + (plan->nqt + plan->nkt) * plan->d.hidden * es};
+    const float* bs[3] = {bias, bias + plan->nqt, bias + plan->nqt + plan->nkt};
+    qkv_status st = check_decode_ptrs(plan, x, ws, bs, d_pos, q, k, v, kv_k, kv_v);
+    if (st != QKV_OK) return st;
+    // only the bulk-copy rings wait on copies: 16-byte aligned rows of at most 16 KB
+    if (!use_vec(plan, x, ws) || static_cast<size_t>(plan->d.hidden) * es > 16384)
+        return fail(QKV_ERR_UNSUPPORTED, "the wait-timeout test needs 16-byte aligned rows of at most 16 KB");
+    DecodeParams p = base_params(plan);
+    p.x = x;
+    for (int i = 0; i < 3; ++i) {
+        p.w[i] = ws[i];
+        p.bias[i] = bs[i];
+    }
+    p.out[0] = q;
+    p.out[1] = k;
+    p.out[2] = v;
+    p.kv_k = kv_k;
+    p.kv_v = kv_v;
+    p.pos = d_pos;
+    p.wait_limit_ns = 1000ull * wait_limit_us;
+    p.withhold_last_copy = 1;
+    cudaError_t e = launch_decode(p, plan->d.w_dtype, 1, kFused, false, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+    return QKV_OK;
 }
 
 extern "C" qkv_status qkv_decode_step_mixed(const qkv_plan* plan, const float* x, const void* wq,

@@ -31,6 +31,11 @@ struct DecodeParams {
     const float* qk_norm_w[2];  // FusedQkvNorm: per-head norm weights of q and k [hd] each
     float qk_eps;               // FusedQkvNorm epsilon
     unsigned int* head_cnt;     // FusedQkvNorm: per-head completion counters [nh + nkv], zero between launches
+    // Test hook of the bounded waits (zero in every product call): a non-zero wait limit
+    // replaces the default, and withhold_last_copy makes the ring producers skip each
+    // CTA's last weight copy, so the wait for it runs out.
+    unsigned long long wait_limit_ns;
+    int32_t withhold_last_copy;
     float inv_freq[QKV_MAX_HEAD_DIM / 2];
 };
 

@@ -28,3 +28,11 @@ def qkv():
     import qkv_rope_kv_gb300 as q
     q.load()
     return q
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """One line with the largest parity errors of every GPU comparison made in this run."""
+    gh = sys.modules.get("gpu_helpers")
+    line = gh.parity_summary() if gh is not None else ""
+    if line:
+        terminalreporter.write_line(line)

@@ -582,4 +582,54 @@ def pin_qknorm_invariants(orc):
     assert st == 1 and not kk4.any() and not vv4.any()
 
 
+def _qkn_decode_case(orc, w_dtype, pos):
+    """The concat FusedQkvNorm stage (projection + norm + rotation + stores) on a hand case,
+    H = 3, hd = 2, two q heads, one kv head, integer weights and x = (1, 2, 3), so that the
+    projection is exact: q heads (1, 1) and (-2, 2), k head (3, -3), v (5, 7)."""
+    W = np.array([[1, 0, 0], [1, 0, 0],       # q head 0: (1, 1), RMS 1
+                  [0, -1, 0], [0, 1, 0],      # q head 1: (-2, 2), RMS 2
+                  [0, 0, 1], [0, 0, -1],      # k head:   (3, -3), RMS 3
+                  [1, 2, 0], [1, 0, 2]],      # v:        (5, 7)
+                 np.float32)
+    if w_dtype == "bf16":
+        W = bf16_bits_exact(W)
+    x = np.array([1, 2, 3], np.float32)
+    bias = np.array([0, 0, 0, 0, 0, 0, 0.5, -1], np.float32)
+    wq, wk = np.float32([1.0, 2.0]), np.float32([3.0, 0.25])
+    kk = np.zeros((4, 2), np.float32)
+    vv = np.zeros((4, 2), np.float32)
+    st, q, k, v = orc.decode_qknorm(W, x, bias, wq, wk, 0.0, 2, 1, 2, 1.0e4, 1.0, pos, kk, vv)
+    return st, q, k, v, kk, vv
+
+
+def pin_qknorm_decode_hand_case(orc):
+    """The concat wrapper of FusedQkvNorm, through the projection: each head normalises to
+    (+-1, +-1), so at pos 0 q = (w_q, -w_q[0], w_q[1]), k = (w_k[0], -w_k[1]) and v = y + b =
+    (5.5, 6), with k and v stored in row 0 only (f32 and bf16 weights).  At pos 2 the pair
+    angle is exactly 2 rad (pair index 0 has frequency freq_scale = 1): each normalised pair
+    (n0, n1) becomes (n0 cos 2 - n1 sin 2, n0 sin 2 + n1 cos 2), stored in row 2."""
+    wq, wk = np.float32([1.0, 2.0]), np.float32([3.0, 0.25])
+    for w_dtype in ("f32", "bf16"):
+        st, q, k, v, kk, vv = _qkn_decode_case(orc, w_dtype, 0)
+        assert st == 0
+        assert np.array_equal(q, np.float32([wq[0], wq[1], -wq[0], wq[1]]))
+        assert np.array_equal(k, np.float32([wk[0], -wk[1]]))
+        assert np.array_equal(v, np.float32([5.5, 6.0]))
+        assert np.array_equal(kk[0], k) and np.array_equal(vv[0], v) and not kk[1:].any() and not vv[1:].any()
+    c, s_ = np.cos(2.0), np.sin(2.0)
+
+    def rot(n0, n1):
+        return np.float32([n0 * c - n1 * s_, n0 * s_ + n1 * c])
+
+    st, q, k, v, kk, vv = _qkn_decode_case(orc, "f32", 2)
+    assert st == 0
+    want_q = np.concatenate([rot(1.0, 2.0), rot(-1.0, 2.0)])
+    want_k = rot(3.0, -0.25)
+    for got, want in ((q, want_q), (k, want_k)):
+        assert np.all(np.abs(f32_bits(got).astype(np.int64) - f32_bits(want).astype(np.int64)) <= 1)
+    assert np.array_equal(v, np.float32([5.5, 6.0]))
+    assert np.array_equal(kk[2], k) and np.array_equal(vv[2], v)
+    assert not kk[[0, 1, 3]].any() and not vv[[0, 1, 3]].any()
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

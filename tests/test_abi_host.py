@@ -274,7 +274,7 @@ def _ctypes_kind(t) -> str:
 
 def _signature_mismatches(lib):
     import re
-    text = re.sub(r"/\*.*?\*/", "", open(q.HEADER).read(), flags=re.S)
+    text = re.sub(r"/\*.*?\*/", "", "".join(open(h).read() for h in q.HEADERS), flags=re.S)
     protos = re.findall(r"\n([A-Za-z_][\w\s\*]*?)\b((?:qkv|kv)_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", text)
     assert sorted(name for _, name, _ in protos) == q.header_entry_points()
     bad = []
@@ -294,3 +294,17 @@ def test_binding_signatures_match_header(lib):
     the number of parameters, each one's kind (pointer, f32, 32/64-bit integer, size_t) and
     the return kind: a drifted declaration would pass garbage without an error."""
     assert _signature_mismatches(lib) == []
+
+
+def test_wait_timeout_hook_guards(lib):
+    """The failure-path test hook rejects a wait limit outside 1 .. 1000 us and null pointers
+    before any CUDA call."""
+    plan = q.qkv_plan_create(64, 2, 1, 32, 1e4, 4)
+    fake = 16 * 64
+    for us, want in ((0, q.QKV_ERR_INVALID_ARG), (1001, q.QKV_ERR_INVALID_ARG)):
+        st = lib.qkv_test_decode_wait_timeout(plan.handle, fake, fake, fake, fake, fake, fake, fake, fake, fake,
+                                              us, None)
+        assert st == want and b"wait_limit_us" in lib.qkv_last_error()
+    st = lib.qkv_test_decode_wait_timeout(plan.handle, None, fake, fake, fake, fake, fake, fake, fake, fake, 100,
+                                          None)
+    assert st == q.QKV_ERR_INVALID_ARG and b"x is null" in lib.qkv_last_error()

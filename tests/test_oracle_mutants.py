@@ -85,6 +85,17 @@ MUTANTS = {
                             "oracle_matvec(Wv, w_is_bf16, x, nkt, hidden, y_scratch + nqt);"),
     "ffn_drops_last_column": ("for (int64_t c = 0; c < H; ++c) {\n                g += (double)rg[c]",
                               "for (int64_t c = 0; c + 1 < H; ++c) {\n                g += (double)rg[c]"),
+    # wiring of the concat FusedQkvNorm wrapper (projection rows, scratch, norm weights, position)
+    "qknorm_wrapper_rows_short": ("const int64_t R = (int64_t)(nh + 2 * nkv) * hd;\n    oracle_matvec(W, w_is_bf16, x, R, hidden, y_scratch);\n    return oracle_qkv_token_qknorm(",
+                                  "const int64_t R = (int64_t)(nh + nkv) * hd;\n    oracle_matvec(W, w_is_bf16, x, R, hidden, y_scratch);\n    return oracle_qkv_token_qknorm("),
+    "qknorm_wrapper_norm_weights_swapped": ("return oracle_qkv_token_qknorm(y_scratch, bias, q_norm_w, k_norm_w,",
+                                            "return oracle_qkv_token_qknorm(y_scratch, bias, k_norm_w, q_norm_w,"),
+    "qknorm_wrapper_scratch_offset": ("return oracle_qkv_token_qknorm(y_scratch, bias,",
+                                      "return oracle_qkv_token_qknorm(y_scratch + hd, bias,"),
+    "qknorm_wrapper_position_dropped": ("eps, nh, nkv, hd, base, freq_scale, pos,\n                                   n_ctx,",
+                                        "eps, nh, nkv, hd, base, freq_scale, 0,\n                                   n_ctx,"),
+    "qknorm_v_from_2nkt": ("v_out[j] = (float)(y[nqt + nkt + j] + (double)bias[nqt + nkt + j]);",
+                           "v_out[j] = (float)(y[2 * nkt + j] + (double)bias[nqt + nkt + j]);"),
 }
 
 

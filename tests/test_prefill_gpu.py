@@ -70,6 +70,17 @@ def check(nh, nkv, hd, got, want, positions, what):
     keep[unchecked] = False
     assert_kv_region(dk[keep], kk[keep], [int(np.sum(keep[:r])) for r in checked], what + " K")
     assert_kv_region(dv[keep], vv[keep], [int(np.sum(keep[:r])) for r in checked], what + " V")
+    # every token's cache rows (checked or not) hold exactly its k and v outputs, rounded
+    # to the cache type (f16 round-to-nearest-even is numpy's float32 -> float16 cast)
+    for t in range(Y.shape[0]):
+        p = int(positions[t])
+        if not 0 <= p < dk.shape[0]:
+            continue
+        ky, vy = Y[t, nqt:nqt + nkt], Y[t, nqt + nkt:]
+        if dk.dtype == np.uint16:
+            ky, vy = ky.astype(np.float16).view(np.uint16), vy.astype(np.float16).view(np.uint16)
+        assert np.array_equal(dk[p].view(ky.dtype), ky), "%s: K row %d is not token %d's k" % (what, p, t)
+        assert np.array_equal(dv[p].view(vy.dtype), vy), "%s: V row %d is not token %d's v" % (what, p, t)
 
 
 SHAPES = [
@@ -146,8 +157,10 @@ def test_prefill_out_of_range_position(orc, qkv):
 
 @pytest.mark.slow
 def test_qwen14b_prefill_nt128_48_layers(orc, qkv):
-    """The 14B prefill workload: every layer on the GPU; the oracle checks all 128
-    tokens of layers 0, 23, 24 and 47 and 8 sampled tokens of every other layer."""
+    """The 14B prefill workload: every layer on the GPU, caches filled with per-slot canaries;
+    the oracle checks all 128 tokens of layers 0, 23, 24 and 47 and 8 sampled tokens of
+    every other layer; on every layer the 3968 rows no token writes keep their canary bits
+    and every token's cache rows hold its own k and v outputs."""
     w = configs.QWEN14B_PREFILL
     R, H = w.rows, w.hidden
     positions = np.arange(w.nt, dtype=np.int32)
@@ -156,11 +169,10 @@ def test_qwen14b_prefill_nt128_48_layers(orc, qkv):
         W = synth.weight_rows(0, layer, 0, R, H, "bf16")
         b = synth.bias(0, layer, R)
         X = synth.prefill_x(0, layer, w.nt, H)
-        kk0 = np.zeros((w.n_ctx, w.nkt), np.uint16)
-        got = run_prefill(H, w.n_head, w.n_head_kv, w.head_dim, w.n_ctx, "f16", X, W, b, positions, kk0,
-                          kk0.copy())
+        kk0, vv0 = canary(w.n_ctx, w.nkt, "f16", 2 * layer), canary(w.n_ctx, w.nkt, "f16", 2 * layer + 1)
+        got = run_prefill(H, w.n_head, w.n_head_kv, w.head_dim, w.n_ctx, "f16", X, W, b, positions, kk0, vv0)
         tokens = range(w.nt) if layer in (0, 23, 24, 47) else sorted(rng.choice(w.nt, 8, replace=False))
-        want = oracle_prefill(orc, X, W, b, positions, w.n_head, w.n_head_kv, w.head_dim, kk0, kk0.copy(),
+        want = oracle_prefill(orc, X, W, b, positions, w.n_head, w.n_head_kv, w.head_dim, kk0, vv0,
                               tokens=tokens)
         check(w.n_head, w.n_head_kv, w.head_dim, got, want, positions, "14B prefill layer %d" % layer)
     assert Q.qkv_check_device_error()[0] == 0
