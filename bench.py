@@ -52,6 +52,8 @@ def parse():
                     help="bound on the oracle's CPU-baseline sample")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU-baseline leg")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="default workload only: skip timing the other configurations")
     ap.add_argument("--layers", type=int, default=None,
                     help="profiling captures only: run the first N layers of the workload "
                          "(the result is not a bench number and says so)")
@@ -151,8 +153,10 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- device model
 
-def build_model(w: configs.Workload, seed: int):
-    """Seeded weights, bias, inputs and zeroed caches for all layers, resident on the device."""
+def build_model(w: configs.Workload, seed: int, sweep: bool = False):
+    """Seeded weights, bias, inputs and zeroed caches for all layers, resident on the device.
+    With ``sweep``, also one input block per decode position of the workload (position and the
+    x of every layer seeded by (layer, position)), resident on the device."""
     import torch
     import qkv_rope_kv_gb300 as Q
 
@@ -200,10 +204,19 @@ def build_model(w: configs.Workload, seed: int):
     h_in[x_off:].view(torch.float32).view(L, w.hidden).copy_(torch.from_numpy(host_x))
     inbuf.copy_(h_in)
     h_out = torch.empty(L, w.rows, dtype=torch.float32).pin_memory()
+    blocks = None
+    if sweep:
+        # block i: [position i | pad | x of every layer at position i], the layout of inbuf
+        hb = torch.zeros(len(w.positions), in_bytes, dtype=torch.uint8)
+        for i, p_ in enumerate(w.positions):
+            hb[i, :4].view(torch.int32)[0] = p_
+            hb[i, x_off:].view(torch.float32).view(L, w.hidden).copy_(
+                torch.from_numpy(np.stack([synth.hidden(seed, l, p_, w.hidden) for l in range(L)])))
+        blocks = hb.to("cuda")
     torch.cuda.synchronize()
     return dict(plans=plans, layer_plans=layer_plans, layers=layers, norms=norms, qk_norms=qk_norms, keep=keep,
                 inbuf=inbuf,
-                dpos=dpos, dx=dx, dout=dout, h_in=h_in, h_out=h_out, in_bytes=in_bytes)
+                dpos=dpos, dx=dx, dout=dout, h_in=h_in, h_out=h_out, in_bytes=in_bytes, blocks=blocks)
 
 
 def time_replays(fn, steps: int, stream, flush=None):
@@ -440,6 +453,131 @@ def workload_config(w: configs.Workload):
 
 # ---------------------------------------------------------------- native arm
 
+def model_graph(m, w, stream):
+    """The whole-model decode graph of a built model (plain, RMSNorm-fused or FusedQkvNorm)."""
+    import torch
+    import qkv_rope_kv_gb300 as Q
+    if w.qknorm:
+        plan0 = m["layer_plans"][0]
+        m["qk_ws"] = torch.zeros(Q.qkv_qknorm_workspace_bytes(plan0) // 4, dtype=torch.int32, device="cuda")
+        return Q.qkv_model_graph_create_qknorm(m["layer_plans"], m["layers"], [a for a, _ in m["qk_norms"]],
+                                               [b for _, b in m["qk_norms"]], w.qk_eps, m["dpos"], m["qk_ws"],
+                                               stream)
+    if w.rmsnorm:
+        return Q.qkv_model_graph_create_rmsnorm(m["layer_plans"], m["layers"], m["norms"], w.rms_eps, m["dpos"],
+                                                stream)
+    return Q.qkv_model_graph_create(m["layer_plans"], m["layers"], m["dpos"], stream)
+
+
+def check_flags(stream, what: str):
+    import qkv_rope_kv_gb300 as Q
+    stream.synchronize()
+    flags, _ = Q.qkv_check_device_error(stream)
+    if flags:
+        raise RuntimeError("device status flags set during %s: %#x" % (what, flags))
+
+
+def roofline_entry(w, layers_per_step: int, elapsed: float, steps: int, launches: int, algo: int):
+    """Throughput fields of one workload entry: layers/s, GB/s and the fractions of the peaks."""
+    peak, peak_kind = measured_peak()
+    per_layer = elapsed / steps / layers_per_step
+    gbs = algo / per_layer / 1e9
+    traffic, kernel = traffic_per_launch(w.name)
+    return {"workload": w.name, "layers": layers_per_step, "steps": steps, "ms_per_step": 1e3 * elapsed / steps,
+            "layers_per_s": layers_per_step * steps / elapsed, "hbm_gbs": gbs, "frac": gbs / peak,
+            "peak": peak, "peak_kind": peak_kind, "frac_of_nominal_8000": gbs / NOMINAL_HBM_GBS,
+            "algo_bytes_per_launch": algo, "traffic": traffic, "traffic_kernel": kernel,
+            "launches_per_step": launches}
+
+
+def decode_workload_entry(w, seed: int, steps: int):
+    """One decode workload timed in this process: its whole-model graph replayed `steps` times
+    (L2 flushed before every step when its weights would stay in L2).  A workload with several
+    positions is a sweep: each step first copies that step's input block (position and the x of
+    every layer, resident on the device) into the graph's input block, inside the timed region,
+    so consecutive steps run consecutive positions."""
+    import torch
+    sweep = len(w.positions) > 1
+    m = build_model(w, seed, sweep=sweep)
+    stream = torch.cuda.Stream()
+    graph = model_graph(m, w, stream)
+    if sweep:
+        blocks, inbuf, P = m["blocks"], m["inbuf"], len(w.positions)
+        step_no = [0]
+
+        def step():
+            with torch.cuda.stream(stream):
+                inbuf.copy_(blocks[step_no[0] % P], non_blocking=True)
+            graph.launch(stream)
+            step_no[0] += 1
+    else:
+        def step():
+            graph.launch(stream)
+    for _ in range(3):
+        step()
+    check_flags(stream, "warm-up of %s" % w.name)
+    flush = l2_flush_buffer(w.n_layers * w.w_bytes())
+    if sweep:
+        step_no[0] = 0
+    elapsed = time_replays(step, steps, stream, flush)
+    check_flags(stream, w.name)
+    e = roofline_entry(w, w.n_layers, elapsed, steps, graph.kernel_count, w.algo_bytes_per_layer())
+    e["config"] = workload_config(w)
+    if sweep:
+        e["sweep"] = ("positions %d..%d in order, one per step (%d sweeps); each step copies its %d-byte input "
+                      "block (position + x of every layer, device resident) into the graph's input block inside "
+                      "the timed region, then replays the %d-launch graph"
+                      % (w.positions[0], w.positions[-1], steps // len(w.positions), m["in_bytes"], w.n_layers))
+    del graph, m
+    torch.cuda.synchronize()
+    return e
+
+
+def prefill_workload_entry(w, seed: int, steps: int, weights=None):
+    """The prefill graph of workload w timed in this process.  `weights`, a list of (W, bias)
+    device tensors per layer, reuses weights already on the device (the 14B decode model's
+    concat weights are the prefill workload's, row for row)."""
+    import torch
+    model = build_prefill(w, seed, weights)
+    stream = torch.cuda.Stream()
+    graph = model["graph_fn"](stream)
+    for _ in range(3):
+        graph.launch(stream)
+    check_flags(stream, "warm-up of %s" % w.name)
+    elapsed = time_replays(lambda: graph.launch(stream), steps, stream)
+    check_flags(stream, w.name)
+    algo_b, algo_f = prefill_algo(w)
+    e = roofline_entry(w, w.n_layers, elapsed, steps, graph.kernel_count, algo_b)
+    e["tflops"] = algo_f / (elapsed / steps / w.n_layers) / 1e12
+    e["algo_flops_per_launch"] = algo_f
+    e["config"] = dict(workload_config(w), nt=w.nt, positions="0..%d" % (w.nt - 1))
+    del graph, model
+    torch.cuda.synchronize()
+    return e
+
+
+def workloads_leg(args, main_entry, main_model):
+    """Every other configuration of the metric, timed in this process after the headline:
+    7B 28 layers, 0.5B single layer (L2 flushed), 0.5B 24-layer sweep over positions 0..127,
+    14B prefill of 128 tokens (on the headline model's weights)."""
+    import torch
+    out = {configs.QWEN14B.name: main_entry}
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    t0 = time.time()
+    plan = [(configs.QWEN7B, max(args.steps, 200)), (configs.QWEN05_SINGLE, max(args.steps, 500)),
+            (configs.QWEN05_SWEEP, 2 * len(configs.QWEN05_SWEEP.positions))]
+    for w, steps in plan:
+        out[w.name] = decode_workload_entry(w, 0, steps)
+    weights = [(main_model["keep"][4 * l], main_model["keep"][4 * l + 1]) for l in range(configs.QWEN14B.n_layers)]
+    out[configs.QWEN14B_PREFILL.name] = prefill_workload_entry(configs.QWEN14B_PREFILL, 0, max(args.steps, 20),
+                                                               weights)
+    clk = clocks.stop()
+    out["clocks"] = clk
+    out["wall_s"] = time.time() - t0
+    return out
+
+
 def native_arm(args, w):
     import torch
     import qkv_rope_kv_gb300 as Q
@@ -455,17 +593,7 @@ def native_arm(args, w):
     seed = rank  # each replica runs its own seeded model
     m = build_model(w, seed)
     stream = torch.cuda.Stream()
-    if w.qknorm:
-        plan0 = m["layer_plans"][0]
-        m["qk_ws"] = torch.zeros(Q.qkv_qknorm_workspace_bytes(plan0) // 4, dtype=torch.int32, device="cuda")
-        graph = Q.qkv_model_graph_create_qknorm(m["layer_plans"], m["layers"], [a for a, _ in m["qk_norms"]],
-                                                [b for _, b in m["qk_norms"]], w.qk_eps, m["dpos"], m["qk_ws"],
-                                                stream)
-    elif w.rmsnorm:
-        graph = Q.qkv_model_graph_create_rmsnorm(m["layer_plans"], m["layers"], m["norms"], w.rms_eps, m["dpos"],
-                                                 stream)
-    else:
-        graph = Q.qkv_model_graph_create(m["layer_plans"], m["layers"], m["dpos"], stream)
+    graph = model_graph(m, w, stream)
     kernels = graph.kernel_count
 
     for _ in range(max(args.warmup, 3)):
@@ -513,6 +641,14 @@ def native_arm(args, w):
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline_leg(w, seed, args.cpu_seconds, "%s at pos %d" % (w.name, w.positions[0]))
 
+    workloads = None
+    if world == 1 and w.name == configs.QWEN14B.name and not args.no_workloads:
+        main_entry = roofline_entry(w, w.n_layers, elapsed, args.steps, kernels, algo)
+        main_entry["config"] = workload_config(w)
+        main_entry["note"] = "the headline line's own measurement"
+        del graph
+        workloads = workloads_leg(args, main_entry, m)
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": layers_per_s, "unit": "layers/s", "n_gpus": world,
@@ -532,6 +668,8 @@ def native_arm(args, w):
             "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": kernels * args.steps,
             "launches_per_step": kernels, "clocks": clk,
         }
+        if workloads is not None:
+            line["workloads"] = workloads
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -544,6 +682,38 @@ def prefill_algo(w: configs.Workload):
               + 2 * w.nt * w.nkt * w.kv_elem_bytes())
     flops = 2 * w.nt * w.rows * w.hidden
     return bytes_, flops
+
+
+def build_prefill(w, seed: int, weights=None):
+    """Seeded prefill inputs of every layer on the device (X of nt tokens, positions 0..nt-1,
+    zeroed caches, Y) and a function that captures the prefill graph on a stream.  `weights`:
+    per-layer (W, bias) device tensors to reuse, else generated from the same seeds."""
+    import torch
+    import qkv_rope_kv_gb300 as Q
+    plan = Q.qkv_plan_create(w.hidden, w.n_head, w.n_head_kv, w.head_dim, w.theta, w.n_ctx,
+                             w_dtype=Q.QKV_BF16, kv_dtype=Q.QKV_F16 if w.kv_dtype == "f16" else Q.QKV_F32,
+                             freq_scale=w.freq_scale)
+    positions = torch.arange(w.nt, dtype=torch.int32, device="cuda")
+    kvt = torch.int16 if w.kv_dtype == "f16" else torch.float32
+    layers = []
+    hostW = np.empty((w.rows, w.hidden), np.uint16)
+    for l in range(w.n_layers):
+        if weights is None:
+            synth.weight_rows(seed, l, 0, w.rows, w.hidden, "bf16", out=hostW)
+            dW = torch.from_numpy(hostW.view(np.int16)).to("cuda")
+            db = torch.from_numpy(synth.bias(seed, l, w.rows)).to("cuda")
+        else:
+            dW, db = weights[l]
+            assert tuple(dW.shape) == (w.rows, w.hidden) and dW.element_size() == 2
+        layers.append(dict(
+            X=torch.from_numpy(synth.prefill_x(seed, l, w.nt, w.hidden).view(np.int16)).to("cuda"),
+            w=dW, bias=db, positions=positions,
+            Y=torch.empty(w.nt, w.rows, dtype=torch.float32, device="cuda"),
+            kv_k=torch.zeros(w.n_ctx, w.nkt, dtype=kvt, device="cuda"),
+            kv_v=torch.zeros(w.n_ctx, w.nkt, dtype=kvt, device="cuda")))
+    torch.cuda.synchronize()
+    return {"plan": plan, "layers": layers,
+            "graph_fn": lambda stream: Q.qkv_prefill_graph_create([plan] * w.n_layers, layers, w.nt, stream)}
 
 
 def prefill_arm(args, w):
@@ -559,25 +729,8 @@ def prefill_arm(args, w):
         torch.cuda.set_device(0)
     Q.load()
     seed = rank
-    plan = Q.qkv_plan_create(w.hidden, w.n_head, w.n_head_kv, w.head_dim, w.theta, w.n_ctx,
-                             w_dtype=Q.QKV_BF16, kv_dtype=Q.QKV_F16 if w.kv_dtype == "f16" else Q.QKV_F32,
-                             freq_scale=w.freq_scale)
-    positions = torch.arange(w.nt, dtype=torch.int32, device="cuda")
-    kvt = torch.int16 if w.kv_dtype == "f16" else torch.float32
-    layers = []
-    hostW = np.empty((w.rows, w.hidden), np.uint16)
-    for l in range(w.n_layers):
-        synth.weight_rows(seed, l, 0, w.rows, w.hidden, "bf16", out=hostW)
-        layers.append(dict(
-            X=torch.from_numpy(synth.prefill_x(seed, l, w.nt, w.hidden).view(np.int16)).to("cuda"),
-            w=torch.from_numpy(hostW.view(np.int16)).to("cuda"),
-            bias=torch.from_numpy(synth.bias(seed, l, w.rows)).to("cuda"),
-            positions=positions,
-            Y=torch.empty(w.nt, w.rows, dtype=torch.float32, device="cuda"),
-            kv_k=torch.zeros(w.n_ctx, w.nkt, dtype=kvt, device="cuda"),
-            kv_v=torch.zeros(w.n_ctx, w.nkt, dtype=kvt, device="cuda")))
     stream = torch.cuda.Stream()
-    graph = Q.qkv_prefill_graph_create([plan] * w.n_layers, layers, w.nt, stream)
+    graph = build_prefill(w, seed)["graph_fn"](stream)
     for _ in range(max(args.warmup, 3)):
         graph.launch(stream)
     stream.synchronize()

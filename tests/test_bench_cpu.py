@@ -43,3 +43,20 @@ def test_traffic_record_keys_ignore_comments(tmp_path, monkeypatch):
     assert bench.source_hash("k.cu") == h0
     src.write_text("// header\nint f(int a) {  // trailing\n  /* block\n comment */ return a + 2;\n}\n")
     assert bench.source_hash("k.cu") != h0
+
+
+def test_roofline_entry_arithmetic():
+    """Workload entries: layers/s, GB/s and the two fractions follow from the elapsed time, the
+    step count and the algorithmic bytes per launch."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from qkv_rope_kv_gb300 import configs
+    w = configs.QWEN7B
+    algo = w.algo_bytes_per_layer()
+    e = bench.roofline_entry(w, w.n_layers, 0.5, 1000, w.n_layers, algo)
+    assert abs(e["layers_per_s"] - w.n_layers * 1000 / 0.5) < 1e-6
+    per_layer = 0.5 / 1000 / w.n_layers
+    assert abs(e["hbm_gbs"] - algo / per_layer / 1e9) < 1e-6
+    assert abs(e["frac"] - e["hbm_gbs"] / e["peak"]) < 1e-12
+    assert abs(e["frac_of_nominal_8000"] - e["hbm_gbs"] / 8000.0) < 1e-12
+    assert e["launches_per_step"] == w.n_layers and e["workload"] == w.name

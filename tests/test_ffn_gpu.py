@@ -7,7 +7,7 @@ layers), every layer against the oracle."""
 import numpy as np
 import pytest
 
-from gpu_helpers import assert_f32_close, to_dev, to_host
+from gpu_helpers import assert_product_close, to_dev, to_host
 from qkv_rope_kv_gb300 import configs, synth
 
 pytestmark = pytest.mark.gpu
@@ -25,6 +25,13 @@ SHAPES = [
     (8, 5, "bf16"),          # 16-byte rows
     (2048, 3001, "f32"),     # 8 KB f32 rows: one CTA per SM, ragged last unit
 ]
+
+
+def factors(orc, W, x, nf):
+    """The oracle's factors of each output: silu(gate_i) and up_i (double), for the floor of the
+    product rule."""
+    y = orc.matvec(W, x)
+    return np.array([orc.silu(v) for v in y[:nf]]), y[nf:]
 
 
 def ffn_inputs(H, nf, wdt, layer):
@@ -51,7 +58,7 @@ def test_ffn_matches_oracle(orc, qkv, shape):
     W, x = ffn_inputs(H, nf, wdt, layer=2)
     got = run_step(qkv, H, nf, wdt, W, x)
     want = orc.ffn_swiglu(W, x)
-    assert_f32_close(got, want, "ffn %s" % (shape,))
+    assert_product_close(got, want, *factors(orc, W, x, nf), "ffn %s" % (shape,))
 
 
 def test_ffn_graph_equals_steps_bitwise(qkv):
@@ -97,7 +104,7 @@ def test_ffn_model_graph_full_size(orc, qkv, w):
     for l in range(L):
         synth.ffn_weight_rows(SEED, l, 0, 2 * w.n_ff, w.hidden, w.w_dtype, out=hostW)
         x = synth.hidden(SEED, 100 + l, 0, w.hidden)
-        want.append(orc.ffn_swiglu(hostW, x))
+        want.append((orc.ffn_swiglu(hostW, x),) + factors(orc, hostW, x, w.n_ff))
         dW = to_dev(hostW)
         dx[l].copy_(to_dev(x))
         keep.append(dW)
@@ -112,7 +119,7 @@ def test_ffn_model_graph_full_size(orc, qkv, w):
     assert flags == 0
     got = to_host(dout)
     for l in range(L):
-        assert_f32_close(got[l], want[l], "%s layer %d" % (w.name, l))
+        assert_product_close(got[l], *want[l], "%s layer %d" % (w.name, l))
     for l in (0, L - 1):
         o = torch.full((w.n_ff,), float("nan"), dtype=torch.float32, device="cuda")
         qkv.qkv_ffn_step(w.hidden, w.n_ff, dt, dx[l], keep[l], o, stream=stream.cuda_stream)

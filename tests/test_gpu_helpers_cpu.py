@@ -71,3 +71,18 @@ def test_kv_region_untouched_rows_bit_exact():
     n0 = len(gh.RECORDS)
     gh.assert_kv_region(want.copy(), want, None, "untouched")
     assert "(4 rows)" in gh.parity_summary(gh.RECORDS[n0:])
+
+
+def test_product_rule_floor_from_factors():
+    """o = s * u: where u is tiny and s large, the floor comes from |s| rms(u), so an absolute
+    error of 0.5e-4 * that passes; twice the bound fails."""
+    s = np.array([3.0, 0.5, 1.0, 2.0])
+    u = np.array([1e-4, 1.0, -1.0, 0.5])
+    o = s * u
+    fl = gh.RMS_FLOOR * (np.abs(s) * np.sqrt(np.mean(u * u)) + np.sqrt(np.mean(s * s)) * np.abs(u))
+    g = o.copy()
+    g[0] += 0.5e-4 * fl[0]
+    gh.assert_product_close(g.astype(np.float32), o.astype(np.float32), s, u, "inside")
+    g[0] = o[0] + 2e-4 * fl[0]
+    with pytest.raises(AssertionError):
+        gh.assert_product_close(g.astype(np.float32), o.astype(np.float32), s, u, "outside")

@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 
 import qkv_rope_kv_gb300 as Q
-from gpu_helpers import assert_f32_close, assert_kv_region, canary, to_dev, to_host
+from gpu_helpers import PREFILL_RMS_FLOOR, assert_f32_close, assert_kv_region, canary, to_dev, to_host
 from qkv_rope_kv_gb300 import configs, synth
 
 pytestmark = pytest.mark.gpu
@@ -59,17 +59,19 @@ def check(nh, nkv, hd, got, want, positions, what):
     nqt, nkt = nh * hd, nkv * hd
     for t, (st, y) in res.items():
         assert st == 0
-        assert_f32_close(Y[t, :nqt], y[:nqt], "%s token %d q" % (what, t))
-        assert_f32_close(Y[t, nqt:nqt + nkt], y[nqt:nqt + nkt], "%s token %d k" % (what, t))
-        assert_f32_close(Y[t, nqt + nkt:], y[nqt + nkt:], "%s token %d v" % (what, t))
+        assert_f32_close(Y[t, :nqt], y[:nqt], "%s token %d q" % (what, t), floor=PREFILL_RMS_FLOOR)
+        assert_f32_close(Y[t, nqt:nqt + nkt], y[nqt:nqt + nkt], "%s token %d k" % (what, t),
+                         floor=PREFILL_RMS_FLOOR)
+        assert_f32_close(Y[t, nqt + nkt:], y[nqt + nkt:], "%s token %d v" % (what, t), floor=PREFILL_RMS_FLOOR)
     # rows of every token were written; compare the checked tokens' rows and require
     # every row that no token writes to keep its bits
     checked = [int(positions[t]) for t in res]
     unchecked = sorted(set(int(p) for p in positions) - set(checked))
     keep = np.ones(dk.shape[0], bool)
     keep[unchecked] = False
-    assert_kv_region(dk[keep], kk[keep], [int(np.sum(keep[:r])) for r in checked], what + " K")
-    assert_kv_region(dv[keep], vv[keep], [int(np.sum(keep[:r])) for r in checked], what + " V")
+    rows = [int(np.sum(keep[:r])) for r in checked]
+    assert_kv_region(dk[keep], kk[keep], rows, what + " K", floor=PREFILL_RMS_FLOOR)
+    assert_kv_region(dv[keep], vv[keep], rows, what + " V", floor=PREFILL_RMS_FLOOR)
     # every token's cache rows (checked or not) hold exactly its k and v outputs, rounded
     # to the cache type (f16 round-to-nearest-even is numpy's float32 -> float16 cast)
     for t in range(Y.shape[0]):
@@ -124,7 +126,8 @@ def test_prefill_single_token_equals_decode(orc, qkv):
     x = (X[0].astype(np.uint32) << 16).view(np.float32)
     kk, vv = kk0.copy(), kk0.copy()
     st, q, k, v = orc.decode(W, x, b, nh, nkv, hd, 1e6, 1.0, pos, kk, vv)
-    assert_f32_close(got[0][0], np.concatenate([q, k, v]), "nt=1 prefill vs decode oracle")
+    assert_f32_close(got[0][0], np.concatenate([q, k, v]), "nt=1 prefill vs decode oracle",
+                     floor=PREFILL_RMS_FLOOR)
     # and against the GPU decode kernel on the same inputs
     plan = Q.qkv_plan_create(H, nh, nkv, hd, 1e6, n_ctx, w_dtype=Q.QKV_BF16, kv_dtype=Q.QKV_F16)
     out = torch.empty(R, dtype=torch.float32, device="cuda")
@@ -133,7 +136,7 @@ def test_prefill_single_token_equals_decode(orc, qkv):
     Q.qkv_decode_step(plan, to_dev(x), to_dev(W), to_dev(b), torch.tensor([pos], dtype=torch.int32, device="cuda"),
                       out[:nh * hd], out[nh * hd:(nh + nkv) * hd], out[(nh + nkv) * hd:], dk, dv)
     torch.cuda.synchronize()
-    assert_f32_close(got[0][0], to_host(out), "nt=1 prefill vs GPU decode")
+    assert_f32_close(got[0][0], to_host(out), "nt=1 prefill vs GPU decode", floor=PREFILL_RMS_FLOOR)
 
 
 def test_prefill_out_of_range_position(orc, qkv):
@@ -150,9 +153,9 @@ def test_prefill_out_of_range_position(orc, qkv):
     assert flags & 1 and bad in (9, -2)
     res, kk, vv = oracle_prefill(orc, X, W, b, positions, nh, nkv, hd, kk0, vv0)
     for t in range(nt):
-        assert_f32_close(Y[t], res[t][1], "token %d" % t)
-    assert_kv_region(dk, kk, [1, 3], "K")
-    assert_kv_region(dv, vv, [1, 3], "V")
+        assert_f32_close(Y[t], res[t][1], "token %d" % t, floor=PREFILL_RMS_FLOOR)
+    assert_kv_region(dk, kk, [1, 3], "K", floor=PREFILL_RMS_FLOOR)
+    assert_kv_region(dv, vv, [1, 3], "V", floor=PREFILL_RMS_FLOOR)
 
 
 @pytest.mark.slow
