@@ -517,6 +517,41 @@ __device__ __forceinline__ Unit unit_info(int u, int nqt, int nkt, int hd) {
     return t;
 }
 
+// Units of the pair ring (one neox pair per unit), decoded without a runtime division when
+// hd / 2 is a power of two (every Qwen head width): the nqt / 2 q pairs, then the nkt / 2 k
+// pairs, then the v row pairs.  Gives the Unit that unit_info<1> gives.
+struct PairUnits {
+    int uq, uk, half, shift, hd, nkt;
+    __device__ __forceinline__ explicit PairUnits(const DecodeParams& p)
+        : uq(p.nqt >> 1), uk(p.nkt >> 1), half(p.hd >> 1), shift(-1), hd(p.hd), nkt(p.nkt) {
+        int e = 0;
+        while ((1 << e) < half) ++e;
+        if ((1 << e) == half) shift = e;
+    }
+    __device__ __forceinline__ Unit at(int u) const {
+        Unit t;
+        if (u < uq + uk) {
+            t.sec = u < uq ? 0 : 1;
+            const int v = t.sec ? u - uq : u;
+            const int h = shift >= 0 ? (v >> shift) : v / half;
+            t.d = v - h * half;
+            t.r = h * hd + t.d;
+            t.n = 1;
+            t.off = half;
+        } else {
+            t.sec = 2;
+            t.r = 2 * (u - uq - uk);
+            t.n = min(1, (nkt - t.r) >> 1);
+            t.off = t.n;
+            t.d = 0;
+        }
+        return t;
+    }
+};
+
+// Items of the next layer a pair-ring CTA brings into L2 after its own copies have landed.
+constexpr int kNextLayerPrefetchItems = 2;
+
 template <int P = kPairs>
 __host__ __device__ __forceinline__ int unit_count(int nqt, int nkt, int hd) {
     const int per_head = ((hd >> 1) + P - 1) / P;
@@ -643,6 +678,8 @@ __global__ void __launch_bounds__((kGroups * kGroupWarps + 1) * 32, 2)
     // ours before its own griddepcontrol.wait, which waits for this grid to finish.
     griddep_launch_dependents();
 
+    static_assert(kPairs == 1, "the pair ring decodes one neox pair per unit");
+    const PairUnits pu(p);
     if (warp == kConsumerWarps) {
         // ---- producer: one lane issues all bulk copies of this CTA ----
         if (lane == 0) {
@@ -656,7 +693,7 @@ __global__ void __launch_bounds__((kGroups * kGroupWarps + 1) * 32, 2)
                     flag_timeout();
                     break;
                 }
-                const Unit t = unit_info(u_begin + i, p.nqt, p.nkt, p.hd);
+                const Unit t = pu.at(u_begin + i);
                 const unsigned char* w = static_cast<const unsigned char*>(p.w[t.sec]);
                 unsigned char* dst = ring + static_cast<size_t>(s) * stage_bytes;
                 const uint32_t blk = static_cast<uint32_t>(t.n) * row_bytes;
@@ -669,6 +706,19 @@ __global__ void __launch_bounds__((kGroups * kGroupWarps + 1) * 32, 2)
             const int first = issued > stages ? issued - stages : 0;
             for (int i = first; i < issued; ++i)
                 if (!mbar_wait_bounded(&full[i % stages], (i / stages) & 1, limit)) flag_timeout();
+            // In a model graph, the next layer's CTA with this index owns the same units (same
+            // shape): bring its first items into L2 now, while this CTA's consumers finish and
+            // the SM changes hands, so its first copies are L2 hits (7B graph +8 %).
+            if (p.next_w[0] != nullptr) {
+                const int npf = n < kNextLayerPrefetchItems ? n : kNextLayerPrefetchItems;
+                for (int i = 0; i < npf; ++i) {
+                    const Unit t = pu.at(u_begin + i);
+                    const unsigned char* w = static_cast<const unsigned char*>(p.next_w[t.sec]);
+                    const uint32_t blk = static_cast<uint32_t>(t.n) * row_bytes;
+                    bulk_prefetch_l2(w + static_cast<size_t>(t.r) * row_bytes, blk);
+                    bulk_prefetch_l2(w + static_cast<size_t>(t.r + t.off) * row_bytes, blk);
+                }
+            }
         }
         return;
     }
@@ -698,7 +748,7 @@ __global__ void __launch_bounds__((kGroups * kGroupWarps + 1) * 32, 2)
             if (lane == 0) flag_timeout();
             break;
         }
-        const Unit t = unit_info(u_begin + i, p.nqt, p.nkt, p.hd);
+        const Unit t = pu.at(u_begin + i);
         const unsigned char* st = ring + static_cast<size_t>(s) * stage_bytes;
         const uint32_t blk = static_cast<uint32_t>(t.n) * row_bytes;
         for (int j = 0; j < t.n; ++j) {

@@ -88,8 +88,10 @@ int use_vec(const qkv_plan* plan, const float* x, const void* const w[3]) {
 qkv_status run_decode(const qkv_plan* plan, const float* x, const void* const w[3],
                       const float* const b[3], const int32_t* d_pos, float* q, float* k, float* v,
                       void* kv_k, void* kv_v, bool pdl, cudaStream_t s, const float* norm_w = nullptr,
-                      float norm_eps = 0.f) {
+                      float norm_eps = 0.f, const void* const* next_w = nullptr) {
     DecodeParams p = base_params(plan);
+    if (next_w != nullptr)
+        for (int i = 0; i < 3; ++i) p.next_w[i] = next_w[i];
     p.norm_w = norm_w;
     p.norm_eps = norm_eps;
     p.x = x;
@@ -729,8 +731,16 @@ qkv_status model_graph_create(const qkv_plan* const* plans, int32_t n_layers, co
             bs[1] = L.bias_k;
             bs[2] = L.bias_v;
         }
+        // the next layer's weights, when it has this layer's shape, as an L2 prefetch hint
+        const void* nws[3] = {nullptr, nullptr, nullptr};
+        if (i + 1 < n_layers) {
+            const qkv_plan* q = plans[i + 1];
+            const float* nbs[3];
+            if (q->d.hidden == p->d.hidden && q->nqt == p->nqt && q->nkt == p->nkt && q->d.w_dtype == p->d.w_dtype)
+                layer_sections(q, layers[i + 1], nws, nbs);
+        }
         st = run_decode(p, L.x, ws, bs, d_pos, L.q, L.k, L.v, L.kv_k, L.kv_v, i > 0, s,
-                        norm_w ? norm_w[i] : nullptr, norm_eps);
+                        norm_w ? norm_w[i] : nullptr, norm_eps, nws[0] != nullptr ? nws : nullptr);
     }
     return finish_capture(s, st, out);
 }

@@ -31,6 +31,10 @@ struct DecodeParams {
     const float* qk_norm_w[2];  // FusedQkvNorm: per-head norm weights of q and k [hd] each
     float qk_eps;               // FusedQkvNorm epsilon
     unsigned int* head_cnt;     // FusedQkvNorm: per-head completion counters [nh + nkv], zero between launches
+    // Weight sections of the next layer of a model graph when it has this layer's shape, else
+    // null: a read-only L2 prefetch hint (the pair ring brings its first items into L2 while
+    // this layer finishes); no result depends on it.
+    const void* next_w[3];
     // Test hook of the bounded waits (zero in every product call): a non-zero wait limit
     // replaces the default, and withhold_last_copy makes the ring producers skip each
     // CTA's last weight copy, so the wait for it runs out.

@@ -9,8 +9,9 @@ Comparison rules (the tolerance the stage's arithmetic supports):
   * a product of two such values (the FusedFFN output silu(g) * u): the same bound with
     the floor of element i taken from the factors, 1e-2 * (|s_i| rms(u) + rms(s) |u_i|);
   * f16 cache values: the f16 code within 1 ulp of the oracle's code wherever the
-    oracle's f32 value is at or above 1e-2 * rms; below that, within the f32 rule's
-    absolute bound plus one f16 spacing (rounding g and o to f16 can add one).
+    oracle's f32 value is at or above the output's floor (1e-2 * rms, the prefill's 1e-1);
+    below it, within the f32 rule's absolute bound plus one f16 spacing (rounding g and o
+    to f16 can add one).
 Every comparison is recorded (floored error, unfloored elementwise error, f16 codes
 accepted only below the floor and their largest ulp distance), and the session prints
 the maxima at its end.
@@ -110,18 +111,20 @@ def f16_spacing(v) -> np.ndarray:
     return np.ldexp(1.0, (np.maximum(e, -14) - 10).astype(np.int64))
 
 
-def assert_f16_close(got_codes, want_codes, want_f32, what: str, rms: float | None = None):
+def assert_f16_close(got_codes, want_codes, want_f32, what: str, rms: float | None = None,
+                     floor: float = RMS_FLOOR):
     """f16 codes against the oracle's codes; want_f32 is the oracle's f32 value of each
-    element (its magnitude decides the rule), rms the section's RMS (default: of want_f32)."""
+    element (its magnitude decides the rule), rms the section's RMS (default: of want_f32),
+    floor the f32 rule's floor for this output."""
     got_codes = np.asarray(got_codes, np.uint16).ravel()
     want_codes = np.asarray(want_codes, np.uint16).ravel()
     o = np.asarray(want_f32, np.float64).ravel()
     assert o.size == want_codes.size, (what, o.size, want_codes.size)
     rms = _rms(o) if rms is None else rms
     ulp = np.abs(f16_ordered(got_codes) - f16_ordered(want_codes))
-    small = np.abs(o) < RMS_FLOOR * rms
+    small = np.abs(o) < floor * rms
     diff = np.abs(f16_value(got_codes) - f16_value(want_codes))
-    near = small & (diff <= REL_TOL * RMS_FLOOR * rms + f16_spacing(o))
+    near = small & (diff <= REL_TOL * floor * rms + f16_spacing(o))
     ok = (ulp <= 1) | near
     via_floor = near & (ulp > 1)
     _record(kind="f16", what=what, n=int(o.size), max_ulp=int(ulp.max()) if ulp.size else 0,
@@ -130,7 +133,7 @@ def assert_f16_close(got_codes, want_codes, want_f32, what: str, rms: float | No
             max_ulp_at_or_above_floor=int(ulp[~small].max()) if (~small).any() else 0)
     bad = ~ok
     assert not bad.any(), "%s: %d f16 values beyond the rule (max ulp %d, %d of them at or above %g * rms)" % (
-        what, int(bad.sum()), int(ulp.max()), int((bad & ~small).sum()), RMS_FLOOR)
+        what, int(bad.sum()), int(ulp.max()), int((bad & ~small).sum()), floor)
 
 
 def assert_kv_region(got, want, pos, what: str, section_f32=None, floor: float = RMS_FLOOR):
@@ -153,7 +156,7 @@ def assert_kv_region(got, want, pos, what: str, section_f32=None, floor: float =
             assert_f32_close(got[p], want[p], "%s row %d" % (what, p), floor=floor)
         else:
             o32 = section_f32 if (section_f32 is not None and len(rows) == 1) else f16_value(want[p])
-            assert_f16_close(got[p], want[p], o32, "%s row %d" % (what, p))
+            assert_f16_close(got[p], want[p], o32, "%s row %d" % (what, p), floor=floor)
 
 
 def parity_summary(records=None) -> str:
