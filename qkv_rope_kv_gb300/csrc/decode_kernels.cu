@@ -645,10 +645,79 @@ __device__ __forceinline__ void dot2_staged(const unsigned char* row0, const uns
     a1 = warp_sum(__fadd_rn(c1.x, c1.y));
 }
 
-template <typename WT, int MODE, int kGroups>
+// x held in registers (CPL > 0: every lane takes exactly CPL chunks of a row, i.e. the row
+// has 32 * CPL chunks of 16 bytes): each consumer lane loads the x values of its chunks
+// once per launch, so the dot loop reads only weights from shared memory.  That halves the
+// loop's shared-memory reads and roughly doubles a warp's rate (one warp per SM
+// sub-partition: 8.3 -> 16 B/clk on 7 KB rows).  CPL = 0: x stays in shared memory.
+template <typename WT, int CPL>
+struct XRegs {
+    static constexpr int kF2 = sizeof(WT) == 2 ? 4 : 2;  // x pairs per 16-byte chunk
+    float2 v[CPL > 0 ? CPL : 1][kF2];
+};
+
+template <typename WT, int CPL>
+__device__ __forceinline__ void load_xregs(XRegs<WT, CPL>& xr, const float4* xs, int H, int t) {
+    if constexpr (CPL > 0) {
+        const int nch = H / (sizeof(WT) == 2 ? 8 : 4);
+#pragma unroll
+        for (int k = 0; k < CPL; ++k) {
+            const float4 xa = ld_shared_f4(xs + t + 32 * k);
+            xr.v[k][0] = make_float2(xa.x, xa.y);
+            xr.v[k][1] = make_float2(xa.z, xa.w);
+            if constexpr (sizeof(WT) == 2) {
+                const float4 xb = ld_shared_f4(xs + nch + t + 32 * k);
+                xr.v[k][2] = make_float2(xb.x, xb.y);
+                xr.v[k][3] = make_float2(xb.z, xb.w);
+            }
+        }
+    }
+}
+
+// dot2_staged with x from registers: the same chunks in the same order and the same packed
+// FMAs, so the same bits.
+template <typename WT, int CPL>
+__device__ __forceinline__ void dot2_xregs(const unsigned char* row0, const unsigned char* row1,
+                                           const XRegs<WT, CPL>& xr, int t, float& a0, float& a1) {
+    float2 c0 = make_float2(0.f, 0.f), c1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) {
+        const uint4 v0 = ld_shared_v4(row0 + 16 * (t + 32 * k));
+        const uint4 v1 = ld_shared_v4(row1 + 16 * (t + 32 * k));
+        if constexpr (sizeof(WT) == 2) {
+            c0 = __ffma2_rn(bf16x2_to_f32x2(v0.x), xr.v[k][0], c0);
+            c1 = __ffma2_rn(bf16x2_to_f32x2(v1.x), xr.v[k][0], c1);
+            c0 = __ffma2_rn(bf16x2_to_f32x2(v0.y), xr.v[k][1], c0);
+            c1 = __ffma2_rn(bf16x2_to_f32x2(v1.y), xr.v[k][1], c1);
+            c0 = __ffma2_rn(bf16x2_to_f32x2(v0.z), xr.v[k][2], c0);
+            c1 = __ffma2_rn(bf16x2_to_f32x2(v1.z), xr.v[k][2], c1);
+            c0 = __ffma2_rn(bf16x2_to_f32x2(v0.w), xr.v[k][3], c0);
+            c1 = __ffma2_rn(bf16x2_to_f32x2(v1.w), xr.v[k][3], c1);
+        } else {
+            c0 = __ffma2_rn(make_float2(__uint_as_float(v0.x), __uint_as_float(v0.y)), xr.v[k][0], c0);
+            c1 = __ffma2_rn(make_float2(__uint_as_float(v1.x), __uint_as_float(v1.y)), xr.v[k][0], c1);
+            c0 = __ffma2_rn(make_float2(__uint_as_float(v0.z), __uint_as_float(v0.w)), xr.v[k][1], c0);
+            c1 = __ffma2_rn(make_float2(__uint_as_float(v1.z), __uint_as_float(v1.w)), xr.v[k][1], c1);
+        }
+    }
+    a0 = warp_sum(__fadd_rn(c0.x, c0.y));
+    a1 = warp_sum(__fadd_rn(c1.x, c1.y));
+}
+
+// Chunks per lane of a row of H elements when they divide evenly among 32 lanes and a
+// register-resident x is compiled for that count, else 0.
+template <typename WT>
+__host__ __device__ __forceinline__ int chunks_per_lane(int H) {
+    const int per = sizeof(WT) == 2 ? 8 : 4;
+    if (H % per != 0 || (H / per) % 32 != 0) return 0;
+    return H / per / 32;
+}
+
+template <typename WT, int MODE, int kGroups, int CPL>
 __global__ void __launch_bounds__((kGroups * kGroupWarps + 1) * 32, 2)
     qkv_decode_tma_kernel(const __grid_constant__ DecodeParams p, int stages, uint32_t stage_bytes,
                           uint32_t x_bytes, int skew) {
+    static_assert(CPL == 0 || kGroupWarps == 1, "register-resident x needs one-warp groups");
     constexpr int kConsumerWarps = kGroups * kGroupWarps;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float2 cs_s[QKV_MAX_HEAD_DIM / 2];  // (cos, sin) of each pair index at pos
@@ -739,6 +808,8 @@ __global__ void __launch_bounds__((kGroups * kGroupWarps + 1) * 32, 2)
     const float inv = norm_inv(p, kConsumerWarps * 32);
     const bool store = pos_ok(pos, p.n_ctx);
     if (MODE == kFused && !store && blockIdx.x == 0 && threadIdx.x == 0) flag_bad_pos(pos);
+    XRegs<WT, CPL> xr;
+    load_xregs<WT, CPL>(xr, xs4, p.H, lane);
 
     const int group = warp / kGroupWarps, gw = warp % kGroupWarps;
     const int gt = gw * 32 + lane;  // thread index within the group
@@ -760,7 +831,8 @@ __global__ void __launch_bounds__((kGroups * kGroupWarps + 1) * 32, 2)
                 b1 = __ldg(p.bias[t.sec] + r1);
             }
             float a0, a1;
-            dot2_staged<WT>(st + j * row_bytes, st + blk + j * row_bytes, xs4, p.H, gt, a0, a1);
+            if constexpr (CPL > 0) dot2_xregs<WT, CPL>(st + j * row_bytes, st + blk + j * row_bytes, xr, lane, a0, a1);
+            else dot2_staged<WT>(st + j * row_bytes, st + blk + j * row_bytes, xs4, p.H, gt, a0, a1);
             const bool last = (j == t.n - 1);
             if constexpr (kGroupWarps > 1) {
                 if (lane == 0) {
@@ -882,7 +954,7 @@ __device__ __forceinline__ void qknorm_finish_head(const DecodeParams& p, int hh
 // pair ring (dot2_staged), so both kernels give the same bits.  With
 // EPI = kEpiSwiglu the same ring runs the FusedFFN: a unit pairs gate rows
 // (i ..) with up rows (nf + i ..), and the second block writes silu(g) * u.
-template <typename WT, int MODE, int kGroups, int EPI>
+template <typename WT, int MODE, int kGroups, int EPI, int CPL>
 __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
     qkv_decode_blk_kernel(const __grid_constant__ DecodeParams p, int stages, uint32_t stage_bytes,
                           uint32_t x_bytes, int max_units, int skew) {
@@ -977,6 +1049,8 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
     const float inv = norm_inv(p, kGroups * 32);
     const bool store = pos_ok(pos, p.n_ctx);
     if (MODE == kFused && EPI != kEpiSwiglu && !store && blockIdx.x == 0 && threadIdx.x == 0) flag_bad_pos(pos);
+    XRegs<WT, CPL> xr;
+    load_xregs<WT, CPL>(xr, xs4, p.H, lane);
 
     for (int i = warp; i < n; i += kGroups) {
         const int st = i % stages;
@@ -994,7 +1068,10 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
             // rows rb + j and rb + j + 1 (the second repeats the first past the block's end)
             const int j1 = (j + 1 < t.n) ? j + 1 : j;
             float a0 = 0.f, a1 = 0.f;
-            if (j < t.n) dot2_staged<WT>(sp + j * row_bytes, sp + j1 * row_bytes, xs4, p.H, lane, a0, a1);
+            if (j < t.n) {
+                if constexpr (CPL > 0) dot2_xregs<WT, CPL>(sp + j * row_bytes, sp + j1 * row_bytes, xr, lane, a0, a1);
+                else dot2_staged<WT>(sp + j * row_bytes, sp + j1 * row_bytes, xs4, p.H, lane, a0, a1);
+            }
             y[j] = a0;
             if (j + 1 < kBlkPairs) y[j + 1] = a1;
         }
@@ -1215,9 +1292,9 @@ RingShape ring_shape(const DecodeParams& p, int groups, int ctas_per_sm, int sme
     return r;
 }
 
-template <typename WT, int MODE, int kGroups>
+template <typename WT, int MODE, int kGroups, int CPL = 0>
 cudaError_t launch_decode_tma(const DecodeParams& p, const RingShape& r, bool pdl, cudaStream_t stream) {
-    auto kernel = qkv_decode_tma_kernel<WT, MODE, kGroups>;
+    auto kernel = qkv_decode_tma_kernel<WT, MODE, kGroups, CPL>;
     const size_t smem = r.x_bytes + static_cast<size_t>(r.stages) * r.stage_bytes + 2 * r.stages * sizeof(uint64_t);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
@@ -1242,7 +1319,7 @@ cudaError_t launch_decode_tma(const DecodeParams& p, const RingShape& r, bool pd
 
 
 // Block ring in a dynamic shared-memory budget (0 stages: does not fit).
-template <typename WT, int MODE, int kGroups, int EPI = kEpiQkv>
+template <typename WT, int MODE, int kGroups, int EPI = kEpiQkv, int CPL = 0>
 cudaError_t launch_decode_blk(const DecodeParams& p, int ctas_per_sm, int smem_kb, bool pdl, cudaStream_t stream,
                               bool& launched) {
     launched = false;
@@ -1267,7 +1344,7 @@ cudaError_t launch_decode_blk(const DecodeParams& p, int ctas_per_sm, int smem_k
     int stages = static_cast<int>((budget - fixed) / stage_bytes);
     stages = stages > kMaxStages ? kMaxStages : stages;
     stages -= stages % kGroups;
-    auto kernel = qkv_decode_blk_kernel<WT, MODE, kGroups, EPI>;
+    auto kernel = qkv_decode_blk_kernel<WT, MODE, kGroups, EPI, CPL>;
     const size_t smem = x_bytes + static_cast<size_t>(stages) * stage_bytes + 2 * stages * sizeof(uint64_t) + tail;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
@@ -1286,6 +1363,41 @@ cudaError_t launch_decode_blk(const DecodeParams& p, int ctas_per_sm, int smem_k
     return cudaLaunchKernelEx(&cfg, kernel, p, stages, stage_bytes, x_bytes, max_units, skew);
 }
 
+// Register-resident x is compiled for the row widths of the Qwen2.5 workloads (chunks per
+// lane 20: H 5120 bf16; 14: H 3584 bf16; 7: H 896 f32) in fused launches; every other
+// width, and projection-only launches, keep x in shared memory (same bits either way).
+template <typename WT, int MODE, int kGroups, int EPI>
+cudaError_t launch_blk_any(const DecodeParams& p, int ctas_per_sm, int smem_kb, bool pdl, cudaStream_t stream,
+                           bool& launched) {
+    if constexpr (MODE == kFused) {
+        const int cpl = chunks_per_lane<WT>(p.H);
+        if constexpr (sizeof(WT) == 2 && kGroups == kGroupsLarge) {
+            if (cpl == 20) return launch_decode_blk<WT, MODE, kGroups, EPI, 20>(p, ctas_per_sm, smem_kb, pdl, stream, launched);
+        }
+        if constexpr (sizeof(WT) == 2 && kGroups == kGroupsSmall && EPI == kEpiSwiglu) {
+            if (cpl == 14) return launch_decode_blk<WT, MODE, kGroups, EPI, 14>(p, ctas_per_sm, smem_kb, pdl, stream, launched);
+        }
+        if constexpr (sizeof(WT) == 4 && kGroups == kGroupsSmall && EPI == kEpiSwiglu) {
+            if (cpl == 7) return launch_decode_blk<WT, MODE, kGroups, EPI, 7>(p, ctas_per_sm, smem_kb, pdl, stream, launched);
+        }
+    }
+    return launch_decode_blk<WT, MODE, kGroups, EPI, 0>(p, ctas_per_sm, smem_kb, pdl, stream, launched);
+}
+
+template <typename WT, int MODE, int kGroups>
+cudaError_t launch_tma_any(const DecodeParams& p, const RingShape& r, bool pdl, cudaStream_t stream) {
+    if constexpr (MODE == kFused) {
+        const int cpl = chunks_per_lane<WT>(p.H);
+        if constexpr (sizeof(WT) == 2 && kGroups == kGroupsSmall) {
+            if (cpl == 14) return launch_decode_tma<WT, MODE, kGroups, 14>(p, r, pdl, stream);
+        }
+        if constexpr (sizeof(WT) == 4 && kGroups == kGroupsTiny) {
+            if (cpl == 7) return launch_decode_tma<WT, MODE, kGroups, 7>(p, r, pdl, stream);
+        }
+    }
+    return launch_decode_tma<WT, MODE, kGroups, 0>(p, r, pdl, stream);
+}
+
 template <typename WT, bool VEC, int MODE>
 cudaError_t launch_decode_t(const DecodeParams& p, bool pdl, cudaStream_t stream) {
     if constexpr (VEC) {
@@ -1293,18 +1405,18 @@ cudaError_t launch_decode_t(const DecodeParams& p, bool pdl, cudaStream_t stream
         if (row >= kSmallRowBytes) {
             // rows of >= 8 KB: block ring (one contiguous copy per stage), else the pair ring
             bool launched = false;
-            const cudaError_t e = launch_decode_blk<WT, MODE, kGroupsLarge>(p, QKV_DECODE_LARGE_CTAS,
-                                                                             QKV_DECODE_LARGE_SMEM_KB, pdl, stream,
-                                                                             launched);
+            const cudaError_t e = launch_blk_any<WT, MODE, kGroupsLarge, kEpiQkv>(p, QKV_DECODE_LARGE_CTAS,
+                                                                                   QKV_DECODE_LARGE_SMEM_KB, pdl,
+                                                                                   stream, launched);
             if (launched || e != cudaSuccess) return e;
             const RingShape r = ring_shape<WT>(p, kGroupsLarge, QKV_DECODE_LARGE_CTAS, QKV_DECODE_LARGE_SMEM_KB);
             if (r.stages > 0) return launch_decode_tma<WT, MODE, kGroupsLarge>(p, r, pdl, stream);
         } else if (row < kTinyRowBytes) {
             const RingShape r = ring_shape<WT>(p, kGroupsTiny, kTinyCtas, kTinySmemKb);
-            if (r.stages > 0) return launch_decode_tma<WT, MODE, kGroupsTiny>(p, r, pdl, stream);
+            if (r.stages > 0) return launch_tma_any<WT, MODE, kGroupsTiny>(p, r, pdl, stream);
         } else {
             const RingShape r = ring_shape<WT>(p, kGroupsSmall, QKV_DECODE_SMALL_CTAS, QKV_DECODE_SMALL_SMEM_KB);
-            if (r.stages > 0) return launch_decode_tma<WT, MODE, kGroupsSmall>(p, r, pdl, stream);
+            if (r.stages > 0) return launch_tma_any<WT, MODE, kGroupsSmall>(p, r, pdl, stream);
         }
     }
     auto kernel = qkv_decode_kernel<WT, VEC, MODE>;
@@ -1327,10 +1439,10 @@ cudaError_t launch_ffn_t(const DecodeParams& p, bool pdl, cudaStream_t stream) {
     bool launched = false;
     const cudaError_t e =
         row >= kSmallRowBytes
-            ? launch_decode_blk<WT, kFused, kGroupsLarge, kEpiSwiglu>(p, QKV_DECODE_LARGE_CTAS, QKV_DECODE_LARGE_SMEM_KB,
-                                                                     pdl, stream, launched)
-            : launch_decode_blk<WT, kFused, kGroupsSmall, kEpiSwiglu>(p, QKV_DECODE_SMALL_CTAS, QKV_DECODE_SMALL_SMEM_KB,
-                                                                     pdl, stream, launched);
+            ? launch_blk_any<WT, kFused, kGroupsLarge, kEpiSwiglu>(p, QKV_DECODE_LARGE_CTAS, QKV_DECODE_LARGE_SMEM_KB,
+                                                                  pdl, stream, launched)
+            : launch_blk_any<WT, kFused, kGroupsSmall, kEpiSwiglu>(p, QKV_DECODE_SMALL_CTAS, QKV_DECODE_SMALL_SMEM_KB,
+                                                                  pdl, stream, launched);
     if (e != cudaSuccess) return e;
     return launched ? cudaSuccess : cudaErrorNotSupported;
 }
@@ -1341,10 +1453,10 @@ cudaError_t launch_qknorm_t(const DecodeParams& p, bool pdl, cudaStream_t stream
     bool launched = false;
     const cudaError_t e =
         row >= kSmallRowBytes
-            ? launch_decode_blk<WT, kFused, kGroupsLarge, kEpiQkvNorm>(p, QKV_DECODE_LARGE_CTAS,
-                                                                      QKV_DECODE_LARGE_SMEM_KB, pdl, stream, launched)
-            : launch_decode_blk<WT, kFused, kGroupsSmall, kEpiQkvNorm>(p, QKV_DECODE_SMALL_CTAS,
-                                                                      QKV_DECODE_SMALL_SMEM_KB, pdl, stream, launched);
+            ? launch_blk_any<WT, kFused, kGroupsLarge, kEpiQkvNorm>(p, QKV_DECODE_LARGE_CTAS,
+                                                                   QKV_DECODE_LARGE_SMEM_KB, pdl, stream, launched)
+            : launch_blk_any<WT, kFused, kGroupsSmall, kEpiQkvNorm>(p, QKV_DECODE_SMALL_CTAS,
+                                                                   QKV_DECODE_SMALL_SMEM_KB, pdl, stream, launched);
     if (e != cudaSuccess) return e;
     return launched ? cudaSuccess : cudaErrorNotSupported;
 }
