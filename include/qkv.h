@@ -279,7 +279,11 @@ qkv_status qkv_model_graph_launch(qkv_graph* graph, void* stream);
 /* Copy-in, replay, copy-out on `stream`, for callers holding host buffers:
  * in_bytes from h_in (host, ideally pinned) to d_in, one replay, then
  * out_bytes from d_out to h_out.  Returns after enqueueing (synchronise
- * `stream` before reading h_out).  Either byte count may be 0. */
+ * `stream` before reading h_out; keep h_in unchanged until then).  Either
+ * byte count may be 0.  The input copy runs on a stream the graph owns
+ * (created on the first call): it waits for the previous replay of this
+ * graph, so it overlaps the previous call's output copy, and the replay waits
+ * for it; the replay and the output copy run on `stream`. */
 qkv_status qkv_model_graph_run_host(qkv_graph* graph, const void* h_in, void* d_in,
                                     size_t in_bytes, const void* d_out, void* h_out,
                                     size_t out_bytes, void* stream);

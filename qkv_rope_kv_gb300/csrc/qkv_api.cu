@@ -586,6 +586,15 @@ struct qkv_graph {
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
     int32_t kernels = 0;
+    // qkv_model_graph_run_host: the host-to-device copy runs on a stream of the graph's own,
+    // after the previous replay (which reads the input block) and beside the previous
+    // device-to-host copy, which stays on the caller's stream.
+    cudaStream_t copy_in = nullptr;
+    cudaEvent_t replayed = nullptr;  // the last replay enqueued by run_host
+    cudaEvent_t copied_in = nullptr;
+    cudaEvent_t copied_out = nullptr;  // the last output copy enqueued by run_host
+    bool replayed_once = false;
+    bool copied_out_once = false;
 };
 
 namespace {
@@ -858,15 +867,40 @@ extern "C" qkv_status qkv_model_graph_run_host(qkv_graph* g, const void* h_in, v
     REQUIRE(out_bytes == 0 || (h_out && d_out), "null output buffer");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
+    if (!g->copy_in) {
+        e = cudaStreamCreateWithFlags(&g->copy_in, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&g->replayed, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&g->copied_in, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&g->copied_out, cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(e, "creating the graph's copy stream");
+    }
     if (in_bytes) {
-        e = cudaMemcpyAsync(d_in, h_in, in_bytes, cudaMemcpyHostToDevice, s);
+        // The input block may be overwritten once the previous replay has read it; the
+        // previous call's device-to-host copy (on the caller's stream) runs meanwhile.
+        if (g->replayed_once) {
+            e = cudaStreamWaitEvent(g->copy_in, g->replayed, 0);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
+        }
+        e = cudaMemcpyAsync(d_in, h_in, in_bytes, cudaMemcpyHostToDevice, g->copy_in);
+        if (e == cudaSuccess) e = cudaEventRecord(g->copied_in, g->copy_in);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, g->copied_in, 0);
         if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
+    }
+    if (g->copied_out_once) {
+        // the replay overwrites the outputs the previous call copies out (whatever its stream)
+        e = cudaStreamWaitEvent(s, g->copied_out, 0);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
     }
     e = cudaGraphLaunch(g->exec, s);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGraphLaunch");
+    e = cudaEventRecord(g->replayed, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    g->replayed_once = true;
     if (out_bytes) {
         e = cudaMemcpyAsync(h_out, d_out, out_bytes, cudaMemcpyDeviceToHost, s);
+        if (e == cudaSuccess) e = cudaEventRecord(g->copied_out, s);
         if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy");
+        g->copied_out_once = true;
     }
     return QKV_OK;
 }
@@ -879,6 +913,13 @@ extern "C" qkv_status qkv_model_graph_kernel_count(const qkv_graph* g, int32_t* 
 
 extern "C" void qkv_model_graph_destroy(qkv_graph* g) {
     if (!g) return;
+    if (g->copy_in) {
+        cudaStreamSynchronize(g->copy_in);
+        cudaStreamDestroy(g->copy_in);
+    }
+    if (g->replayed) cudaEventDestroy(g->replayed);
+    if (g->copied_in) cudaEventDestroy(g->copied_in);
+    if (g->copied_out) cudaEventDestroy(g->copied_out);
     if (g->exec) cudaGraphExecDestroy(g->exec);
     if (g->graph) cudaGraphDestroy(g->graph);
     delete g;

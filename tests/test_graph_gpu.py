@@ -227,6 +227,42 @@ def test_run_host_matches_device_replay(orc, qkv):
     assert np.array_equal(h_out.numpy().view(np.uint32), to_host(model.dout).view(np.uint32))
 
 
+def test_run_host_calls_in_a_row(orc, qkv):
+    """Four run_host calls enqueued back to back (each with its own host input and output
+    buffers, one synchronisation at the end): the input copy of a call overlaps the output
+    copy of the one before, and every call's outputs are its own step's, against the
+    oracle.  The position travels in the input block, as in the bench's host path."""
+    import torch
+    w = configs.Workload("small-host-seq", 1024, 8, 2, 64, "bf16", "f16", 64, 3, (9,), mixed_layers=(1,))
+    model = DeviceModel(w)
+    x_off = 256
+    in_bytes = x_off + w.n_layers * w.hidden * 4
+    block = torch.zeros(in_bytes, dtype=torch.uint8, device="cuda")
+    model.dpos = block[:4].view(torch.int32)
+    model.dx = block[x_off:].view(torch.float32).view(w.n_layers, w.hidden)
+    stream = torch.cuda.Stream()
+    g = model.graph(stream)
+    positions = [3, 17, 40, 63]
+    h_ins, h_outs = [], []
+    for p in positions:
+        h = torch.zeros(in_bytes, dtype=torch.uint8)
+        h[:4].view(torch.int32)[0] = p
+        h[x_off:].view(torch.float32).view(w.n_layers, w.hidden).copy_(
+            torch.from_numpy(np.stack([L.x(p) for L in model.layers]).astype(np.float32)))
+        h_ins.append(h.pin_memory())
+        h_outs.append(torch.full((w.n_layers, w.rows), float("nan"), dtype=torch.float32).pin_memory())
+    torch.cuda.synchronize()
+    for h_in, h_out in zip(h_ins, h_outs):
+        g.run_host(h_in, block, model.dout, h_out, stream)
+    stream.synchronize()
+    kv_state = [(k.copy(), v.copy()) for k, v in model.kv0]
+    for p, h_out in zip(positions, h_outs):
+        want = oracle_model_step(orc, model, p, kv_state)
+        check_outputs(model, h_out.numpy(), want, "run_host pos %d" % p)
+    check_caches(model, kv_state, positions, want)
+    assert Q.qkv_check_device_error(stream)[0] == 0
+
+
 def test_qwen7b_28_layers_rmsnorm(orc, qkv):
     _single_step_model(orc, configs.QWEN7B_NORM)
 
