@@ -276,10 +276,26 @@ __device__ __forceinline__ PairTile pair_tile(int tile, const PrefillParams& p) 
     return t;
 }
 
-template <int S>
+// TMEM column of the first accumulator of box A / box B of cluster tile q.  With one W box
+// per cluster (BLOCK: the cluster's tiles are 128 consecutive weight rows, loaded as one
+// 16 KB box per K block in row order), a q/k head of 128 rows holds tile 0 in columns 0-31
+// and 64-95 and tile 1 in 32-63 and 96-127 (the neox partner of row d is d + 64); a head of
+// 64 rows, and the v rows, are tile-contiguous as with one box per 32 rows.
+template <bool BLOCK>
+__device__ __forceinline__ uint32_t tile_col_a(int q, int sec, int hd) {
+    return (BLOCK && sec < 2 && hd == 128) ? static_cast<uint32_t>(q * kBox) : static_cast<uint32_t>(q * kBN);
+}
+template <bool BLOCK>
+__device__ __forceinline__ uint32_t tile_col_b(int q, int sec, int hd) {
+    return (BLOCK && sec < 2 && hd == 128) ? static_cast<uint32_t>(hd / 2 + q * kBox)
+                                           : static_cast<uint32_t>(q * kBN + kBox);
+}
+
+template <int S, bool BLOCK>
 __global__ void __launch_bounds__(kThreads, 1)
     qkv_prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                        const __grid_constant__ CUtensorMap tm_y, const __grid_constant__ PrefillParams p) {
+    static_assert(!BLOCK || S == 2, "one W box per cluster covers two pair tiles");
     using C = Split<S>;
     extern __shared__ unsigned char smem_raw[];
     __shared__ float bias_s[kBN];
@@ -353,12 +369,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(&wfull[s], static_cast<uint32_t>(valid) * C::kWBlk);
             for (int j = 0; j < valid; ++j) {
                 const int kc = (kb0 + j) * kBK;
+                if constexpr (BLOCK) {
+                    // the cluster's two tiles are 128 consecutive rows from the first tile's box A
+                    const PairTile pt = pair_tile(tile0, p);
+                    tma_load_2d(sB + s * C::kWStage + j * C::kWBlk, &tm_w, kc, pt.base + pt.rowA, &wfull[s]);
+                } else {
 #pragma unroll
-                for (int t = 0; t < S; ++t) {
-                    const PairTile pt = pair_tile(tile0 + t, p);
-                    unsigned char* b = sB + s * C::kWStage + j * C::kWBlk + t * kTileBlk;
-                    tma_load_2d(b, &tm_w, kc, pt.base + pt.rowA, &wfull[s]);
-                    tma_load_2d(b + kBoxBytes, &tm_w, kc, pt.base + pt.rowB, &wfull[s]);
+                    for (int t = 0; t < S; ++t) {
+                        const PairTile pt = pair_tile(tile0 + t, p);
+                        unsigned char* b = sB + s * C::kWStage + j * C::kWBlk + t * kTileBlk;
+                        tma_load_2d(b, &tm_w, kc, pt.base + pt.rowA, &wfull[s]);
+                        tma_load_2d(b + kBoxBytes, &tm_w, kc, pt.base + pt.rowB, &wfull[s]);
+                    }
                 }
             }
             ++issued;
@@ -441,8 +463,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int q = 0; q < S; ++q) {
                 if (q == static_cast<int>(rank)) continue;
                 float va[kPc], vb[kPc];
-                tc_ld_cols<kPc>(taddr + q * kBN + c0, va);
-                tc_ld_cols<kPc>(taddr + q * kBN + kBox + c0, vb);
+                tc_ld_cols<kPc>(taddr + tile_col_a<BLOCK>(q, own.sec, p.hd) + c0, va);
+                tc_ld_cols<kPc>(taddr + tile_col_b<BLOCK>(q, own.sec, p.hd) + c0, vb);
                 tc_wait_ld();
                 const uint32_t dst = map_to_rank(xchg + (rank * kBM + tl) * kXchgStride, static_cast<uint32_t>(q));
 #pragma unroll
@@ -457,8 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     float aa[kPc], ab[kPc];  // this thread's pairs: box A and box B values
     if (acc_ready) {
-        tc_ld_cols<kPc>(taddr + rank * kBN + c0, aa);
-        tc_ld_cols<kPc>(taddr + rank * kBN + kBox + c0, ab);
+        tc_ld_cols<kPc>(taddr + tile_col_a<BLOCK>(static_cast<int>(rank), own.sec, p.hd) + c0, aa);
+        tc_ld_cols<kPc>(taddr + tile_col_b<BLOCK>(static_cast<int>(rank), own.sec, p.hd) + c0, ab);
         tc_wait_ld();
         if constexpr (S > 1) {
             // Sum the S K ranges in rank order (the same order in every CTA).
@@ -623,10 +645,10 @@ bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 
 namespace {
 
-template <int S>
+template <int S, bool BLOCK = false>
 cudaError_t launch_split(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const CUtensorMap& tm_y,
                          const PrefillParams& p, int tiles, bool pdl, cudaStream_t stream) {
-    auto kernel = qkv_prefill_kernel<S>;
+    auto kernel = qkv_prefill_kernel<S, BLOCK>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Split<S>::kSmem));
     if (e != cudaSuccess) return e;
@@ -680,16 +702,25 @@ qkv_status launch_prefill(const PrefillParams& p, bool pdl, cudaStream_t stream,
     const int nkb = (p.H + kBK - 1) / kBK;
     int split = QKV_PREFILL_SPLIT;
     while (split > 1 && (tiles % split != 0 || nkb < split)) split >>= 1;
+    // One 16 KB W box per K block and cluster (in place of four 4 KB boxes) when the cluster's
+    // two pair tiles are 128 consecutive rows: whole heads of 64 or 128 rows, and no cluster
+    // across the q|k or k|v boundary.  A bulk tensor load costs about the same time whatever
+    // its size up to ~16-32 KB, so four times fewer, larger boxes stream W about 3x faster.
+    const int tq = p.nqt / kBN, tk = p.nkt / kBN;
+    const bool block = split == 2 && (p.hd == 64 || p.hd == 128) && tq % 2 == 0 && (tq + tk) % 2 == 0;
     CUtensorMap tm_x, tm_w, tm_y;
     if (!encode_f32_2d_store(&tm_y, p.Y, static_cast<uint64_t>(p.nt), static_cast<uint64_t>(R), kBM) ||
         !encode_bf16_2d(&tm_x, p.X, static_cast<uint64_t>(p.nt), static_cast<uint64_t>(p.H), kBM) ||
-        !encode_bf16_2d(&tm_w, p.W, static_cast<uint64_t>(R), static_cast<uint64_t>(p.H), kBox)) {
+        !encode_bf16_2d(&tm_w, p.W, static_cast<uint64_t>(R), static_cast<uint64_t>(p.H),
+                        block ? 2 * kBN : kBox)) {
         *why = "cuTensorMapEncodeTiled failed or is unavailable";
         return QKV_ERR_CUDA;
     }
     cudaError_t e;
     if (split == 4)
         e = launch_split<4>(tm_x, tm_w, tm_y, p, tiles, pdl, stream);
+    else if (split == 2 && block)
+        e = launch_split<2, true>(tm_x, tm_w, tm_y, p, tiles, pdl, stream);
     else if (split == 2)
         e = launch_split<2>(tm_x, tm_w, tm_y, p, tiles, pdl, stream);
     else
