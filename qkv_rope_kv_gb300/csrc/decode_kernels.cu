@@ -419,7 +419,8 @@ __global__ void __launch_bounds__(256) qkv_decode_kernel(const __grid_constant__
 // ---------------------------------------------------------------- bulk-copy pipelined projection
 
 // Persistent variant for 16-byte aligned rows: one CTA per SM owns a
-// contiguous range of row-pair units.  A producer warp streams each unit's two
+// share of the row-pair units (a contiguous range, or for rows under 4 KB units
+// b, b + grid, ...).  A producer warp streams each unit's two
 // rows (2 x H weights) into a ring of shared-memory stages with cp.async.bulk
 // (L2 evict-first: each byte is used once), ahead of the consumers.  Consumer
 // group g (G warps) owns stages g, g + NG, ... and reduces whole units from
@@ -730,9 +731,13 @@ __global__ void __launch_bounds__((kGroups * kGroupWarps + 1) * 32, 2)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int half = p.hd >> 1;
     const int units = unit_count(p.nqt, p.nkt, p.hd);
-    const int u_begin = unit_split(units, blockIdx.x, gridDim.x, skew);
-    const int u_end = unit_split(units, blockIdx.x + 1, gridDim.x, skew);
-    const int n = u_end - u_begin;
+    // Rows under 4 KB (three CTAs per SM) take units b, b + grid, ... (0.5B sweep +2 %); the
+    // 4-8 KB rows keep skewed contiguous shares (strided measured -2 % on the 7B graph).
+    constexpr bool kStrided = kGroups == kGroupsTiny;
+    const int u_step = kStrided ? static_cast<int>(gridDim.x) : 1;
+    const int u_begin = kStrided ? static_cast<int>(blockIdx.x) : unit_split(units, blockIdx.x, gridDim.x, skew);
+    const int n = kStrided ? (units > u_begin ? (units - 1 - u_begin) / static_cast<int>(gridDim.x) + 1 : 0)
+                           : unit_split(units, blockIdx.x + 1, gridDim.x, skew) - u_begin;
     const uint32_t row_bytes = static_cast<uint32_t>(p.H) * sizeof(WT);
 
     if (threadIdx.x == 0) {
@@ -762,7 +767,7 @@ __global__ void __launch_bounds__((kGroups * kGroupWarps + 1) * 32, 2)
                     flag_timeout();
                     break;
                 }
-                const Unit t = pu.at(u_begin + i);
+                const Unit t = pu.at(u_begin + i * u_step);
                 const unsigned char* w = static_cast<const unsigned char*>(p.w[t.sec]);
                 unsigned char* dst = ring + static_cast<size_t>(s) * stage_bytes;
                 const uint32_t blk = static_cast<uint32_t>(t.n) * row_bytes;
@@ -781,7 +786,7 @@ __global__ void __launch_bounds__((kGroups * kGroupWarps + 1) * 32, 2)
             if (p.next_w[0] != nullptr) {
                 const int npf = n < kNextLayerPrefetchItems ? n : kNextLayerPrefetchItems;
                 for (int i = 0; i < npf; ++i) {
-                    const Unit t = pu.at(u_begin + i);
+                    const Unit t = pu.at(u_begin + i * u_step);
                     const unsigned char* w = static_cast<const unsigned char*>(p.next_w[t.sec]);
                     const uint32_t blk = static_cast<uint32_t>(t.n) * row_bytes;
                     bulk_prefetch_l2(w + static_cast<size_t>(t.r) * row_bytes, blk);
@@ -819,7 +824,7 @@ __global__ void __launch_bounds__((kGroups * kGroupWarps + 1) * 32, 2)
             if (lane == 0) flag_timeout();
             break;
         }
-        const Unit t = pu.at(u_begin + i);
+        const Unit t = pu.at(u_begin + i * u_step);
         const unsigned char* st = ring + static_cast<size_t>(s) * stage_bytes;
         const uint32_t blk = static_cast<uint32_t>(t.n) * row_bytes;
         for (int j = 0; j < t.n; ++j) {
@@ -945,8 +950,8 @@ __device__ __forceinline__ void qknorm_finish_head(const DecodeParams& p, int hh
 
 // Block ring: a unit of kBlkPairs neox pairs has two row blocks, (h*hd + d0 ..)
 // and (h*hd + hd/2 + d0 ..); each block is one stage, filled by one contiguous
-// bulk copy.  Item i of a CTA is block (i & 1) of its unit i >> 1 (a contiguous
-// share of all units).  Consumer groups (one warp each) own stages g, g + NG, ...
+// bulk copy.  Item i of a CTA is block (i & 1) of its local unit i >> 1 (see below
+// for which units a CTA takes).  Consumer groups (one warp each) own stages g, g + NG, ...
 // The consumer of a q/k block publishes its biased dot products in shared
 // memory and bumps the unit's counter; the second of the two blocks to finish
 // rotates the unit's pairs and stores them, one pair per lane.  v blocks need
@@ -954,6 +959,10 @@ __device__ __forceinline__ void qknorm_finish_head(const DecodeParams& p, int hh
 // pair ring (dot2_staged), so both kernels give the same bits.  With
 // EPI = kEpiSwiglu the same ring runs the FusedFFN: a unit pairs gate rows
 // (i ..) with up rows (nf + i ..), and the second block writes silu(g) * u.
+// Except with kEpiQkvNorm (whose heads must end up in few CTAs) a CTA takes units
+// b, b + grid, b + 2 grid, ... rather than a contiguous share: in a chained launch
+// the CTAs that start last (the highest block indices) then hold the smaller
+// shares, and every QKV CTA ends on v rows (14B graph +1.6 %, FFN +1 %).
 template <typename WT, int MODE, int kGroups, int EPI, int CPL>
 __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
     qkv_decode_blk_kernel(const __grid_constant__ DecodeParams p, int stages, uint32_t stage_bytes,
@@ -972,10 +981,14 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
     int* cnt = reinterpret_cast<int*>(res + max_units * 2 * kBlkPairs);  // [max_units]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr bool kStrided = EPI != kEpiQkvNorm;
     const int units = blk_unit_count<EPI>(p);
-    const int u_begin = unit_split(units, blockIdx.x, gridDim.x, skew);
-    const int u_end = unit_split(units, blockIdx.x + 1, gridDim.x, skew);
-    const int n = 2 * (u_end - u_begin);
+    const int b = static_cast<int>(blockIdx.x), g = static_cast<int>(gridDim.x);
+    const int u_begin = kStrided ? b : unit_split(units, b, g, skew);
+    const int u_step = kStrided ? g : 1;  // unit of local index ul: u_begin + ul * u_step
+    const int u_end = kStrided ? 0 : unit_split(units, b + 1, g, skew);  // contiguous shares only
+    const int n_units = kStrided ? (units > b ? (units - 1 - b) / g + 1 : 0) : u_end - u_begin;
+    const int n = 2 * n_units;
     const uint32_t row_bytes = static_cast<uint32_t>(p.H) * sizeof(WT);
 
     if (threadIdx.x == 0) {
@@ -1004,7 +1017,7 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
                     flag_timeout();
                     break;
                 }
-                const Unit t = blk_unit<EPI>(u_begin + (i >> 1), p);
+                const Unit t = blk_unit<EPI>(u_begin + (i >> 1) * u_step, p);
                 const int rb = (i & 1) ? t.r + t.off : t.r;
                 const uint32_t bytes = static_cast<uint32_t>(t.n) * row_bytes;
                 const unsigned char* w = static_cast<const unsigned char*>(p.w[t.sec]);
@@ -1026,15 +1039,15 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
     // Biases are parameters, not outputs of an earlier kernel: stage this CTA's
     // share before the dependency wait, so no global load sits in the item loop.
     if (MODE == kFused && EPI != kEpiSwiglu) {
-        const int nb = (u_end - u_begin) * 2 * kBlkPairs;
+        const int nb = n_units * 2 * kBlkPairs;
         for (int e = threadIdx.x; e < nb; e += kGroups * 32) {
             const int j = e % kBlkPairs, blk = (e / kBlkPairs) & 1, ul = e / (2 * kBlkPairs);
-            const Unit t = blk_unit<EPI>(u_begin + ul, p);
+            const Unit t = blk_unit<EPI>(u_begin + ul * u_step, p);
             bias_s[e] = j < t.n ? __ldg(p.bias[t.sec] + (blk ? t.r + t.off : t.r) + j) : 0.f;
         }
     }
     for (int ul = threadIdx.x; 2 * ul < n && ul < kUnitTable; ul += kGroups * 32)
-        unit_s[ul] = pack_unit(blk_unit<EPI>(u_begin + ul, p));
+        unit_s[ul] = pack_unit(blk_unit<EPI>(u_begin + ul * u_step, p));
     prefetch_norm(p, threadIdx.x, kGroups * 32);
     griddep_wait();
     const int pos = (MODE == kFused && EPI != kEpiSwiglu) ? *p.pos : 0;
@@ -1059,7 +1072,7 @@ __global__ void __launch_bounds__((kGroups + 1) * 32, 1)
             break;
         }
         const int ul = i >> 1, blk = i & 1;
-        const Unit t = ul < kUnitTable ? unpack_unit(unit_s[ul]) : blk_unit<EPI>(u_begin + ul, p);
+        const Unit t = ul < kUnitTable ? unpack_unit(unit_s[ul]) : blk_unit<EPI>(u_begin + ul * u_step, p);
         const int rb = blk ? t.r + t.off : t.r;
         const unsigned char* sp = ring + static_cast<size_t>(st) * stage_bytes;
         float y[kBlkPairs];
@@ -1259,8 +1272,9 @@ int sm_count() {
 #endif
 constexpr int kMaxStages = QKV_DECODE_MAX_STAGES;
 // Work skew (percent) of the ring kernels in a chained launch: see unit_split.  The
-// pair ring (rows < 8 KB: 7B-size layers, 8 us each) gains from it (+4 % at 20 on the 7B
-// graph); the block ring's 12-unit shares are too coarse to skew without imbalance.
+// pair ring (rows of 4-8 KB: 7B-size layers, 8 us each) gains from it (+4 % at 20 on the
+// 7B graph); the block ring's 12-unit shares are too coarse to skew without imbalance
+// (the FusedQkvNorm ring keeps even contiguous shares; the others take strided units).
 #ifndef QKV_DECODE_CHAIN_SKEW_PAIR
 #define QKV_DECODE_CHAIN_SKEW_PAIR 20
 #endif
@@ -1336,9 +1350,13 @@ cudaError_t launch_decode_blk(const DecodeParams& p, int ctas_per_sm, int smem_k
     const int grid = units < ctas_max ? units : ctas_max;
     const int skew = pdl ? kChainSkewBlock : 0;
     int max_units = 0;
-    for (int b = 0; b < grid; ++b) {
-        const int nb = unit_split(units, b + 1, grid, skew) - unit_split(units, b, grid, skew);
-        max_units = nb > max_units ? nb : max_units;
+    if (EPI != kEpiQkvNorm) {
+        max_units = (units + grid - 1) / grid;  // units b, b + grid, ...
+    } else {
+        for (int b = 0; b < grid; ++b) {
+            const int nb = unit_split(units, b + 1, grid, skew) - unit_split(units, b, grid, skew);
+            max_units = nb > max_units ? nb : max_units;
+        }
     }
     // per unit: staged biases, published results and a counter
     const size_t tail = static_cast<size_t>(max_units) * (4 * kBlkPairs * sizeof(float) + sizeof(int));
