@@ -145,6 +145,22 @@ def test_prefill_guards(lib):
     assert e.value.status == q.QKV_ERR_UNSUPPORTED
 
 
+def test_prefill_degenerate_token_counts(lib):
+    """nt = 0 is a no-op that succeeds without touching the device; a negative nt is rejected;
+    a head_dim the tensor-core tiles cannot pair (not a multiple of 64) is refused before any
+    launch.  Stand-in addresses: nothing is dereferenced on these paths."""
+    fake = 16 * 64
+    bf16 = q.qkv_plan_create(64, 2, 1, 8, 1e4, 16, w_dtype=q.QKV_BF16)
+    q.qkv_prefill_step(bf16, fake, 0, fake, fake, fake, fake, fake, fake, stream=0)
+    with pytest.raises(q.QkvError) as e:
+        q.qkv_prefill_step(bf16, fake, -1, fake, fake, fake, fake, fake, fake, stream=0)
+    assert e.value.status == q.QKV_ERR_INVALID_ARG
+    with pytest.raises(q.QkvError) as e:
+        q.qkv_prefill_step(bf16, fake, 3, fake, fake, fake, fake, fake, fake, stream=0)
+    assert e.value.status == q.QKV_ERR_UNSUPPORTED
+    assert b"multiple of 64" in lib.qkv_last_error()
+
+
 def test_graph_create_guards(lib):
     p = q.qkv_plan_create(64, 2, 1, 8, 1e4, 16)
     h = ctypes.c_void_p()
