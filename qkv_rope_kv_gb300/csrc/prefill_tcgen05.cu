@@ -23,11 +23,12 @@
 // tile's CTA (distributed shared memory), and CTA r adds the S partials of tile
 // r in rank order, so the result does not depend on which CTA finishes first.
 // All four warps then run the epilogue of tile r, one token per thread: bias,
-// RoPE, Y through shared memory (128-byte swizzle) and two TMA tensor stores,
-// the token's k/v cache rows as 16-byte stores.  Every wait is bounded; on
-// expiry the kernel flags the device status word, drains in-flight copies and
-// MMAs, frees TMEM and returns.  Cluster barriers order the exchange, and a CTA
-// leaves only after the last one, so no peer still reads or writes it.
+// RoPE (its (cos, sin) computed while the K loop runs), Y through shared memory
+// (128-byte swizzle) and two TMA tensor stores, the token's k/v cache rows as
+// 16-byte stores.  Every wait is bounded; on expiry the kernel flags the device
+// status word, drains in-flight copies and MMAs, frees TMEM and returns.  Two
+// cluster barriers order the exchange; after the second no CTA touches a peer's
+// shared memory, so the CTAs of a cluster leave independently.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -357,6 +358,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         // ---- W producer: per K block, the two 32-row boxes of each of the S pair tiles ----
         prefetch_tensormap(&tm_w);
+        {
+            // Warm L2 with this cluster's share of the X rows in this CTA's K range (every X
+            // block is read by all clusters at about the same time, so its first reads would
+            // otherwise wait for HBM together).  A prefetch binds no values: the X loads after
+            // the dependency wait still read what the preceding grid wrote.
+            const int k_lo = kb_lo * kBK, k_n = min(kb_hi * kBK, p.H) - k_lo;
+            const int ncl = static_cast<int>(gridDim.x) / S, cl = static_cast<int>(blockIdx.x) / S;
+            for (int t = m0 + cl; t < min(m0 + kBM, p.nt); t += ncl)
+                bulk_prefetch_l2(p.X + static_cast<size_t>(t) * p.H + k_lo, static_cast<uint32_t>(k_n) * 2u);
+        }
         int issued = 0;
         for (int st = 0; st < n_stages; ++st) {
             const int s = st % C::kWStages;
@@ -438,18 +449,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_commit(done);  // arrives when every MMA issued above has completed
     }
-    __syncwarp();
 
     // ---- partial sums: thread (warp, lane) owns TMEM lane 32*(warp%4) + lane = token m0 + that,
     // and pairs c0 .. c0 + kPc - 1 of the tile (columns c0.. of box A and 32 + c0.. of box B) ----
     constexpr int kPc = kBox / kParts;
+    const int quarter = warp & 3;
+    const int c0 = (warp >> 2) * kPc;
+    const int tl = quarter * 32 + lane;  // this thread's token within the tile
+    const int t = m0 + tl;
+    // The token's position and the (cos, sin) of this thread's pairs, while the K loop runs
+    // (the three lanes with a role above compute theirs after it).
+    const int pos = t < p.nt ? p.positions[t] : 0;
+    float2 cs[kPc];
+    if (own.sec < 2) {
+#pragma unroll
+        for (int i = 0; i < kPc; ++i) cs[i] = rope_cos_sin(pos, freq_s[c0 + i]);
+    }
+    __syncwarp();
     // Warp-uniform: tcgen05.ld below is a warp-collective instruction.
     const bool acc_ready = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(done, 0));
     if (!acc_ready && lane == 0) flag_timeout();
     tc_fence_after();
-    const int quarter = warp & 3;
-    const int c0 = (warp >> 2) * kPc;
-    const int tl = quarter * 32 + lane;  // this thread's token within the tile
     const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     float* xchg = reinterpret_cast<float*>(smem);  // S slots of [128 tokens x kXchgStride], after the K loop
     if constexpr (S > 1) {
@@ -510,11 +530,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---- epilogue of this CTA's tile ----
-    const int t = m0 + tl;
     float* ys = xchg + S * (kXchgSlot / 4);  // Y staging, past the exchange slots
     if (acc_ready) {
         const bool live = t < p.nt;
-        const int pos = live ? p.positions[t] : 0;
         const bool store = live && pos_ok(pos, p.n_ctx);
         if (live && !store && c0 == 0) flag_bad_pos(pos);
         if (own.sec < 2) {
@@ -523,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float x0 = __fadd_rn(aa[i], bias_s[c0 + i]);
                 const float x1 = __fadd_rn(ab[i], bias_s[kBox + c0 + i]);
                 float r0, r1;
-                rope_rotate(x0, x1, rope_theta(pos, freq_s[c0 + i]), r0, r1);
+                rope_rotate_cs(x0, x1, cs[i], r0, r1);
                 aa[i] = r0;
                 ab[i] = r1;
             }
@@ -584,9 +602,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_store_2d(&tm_y, ys + kBM * kBox, own.base + own.rowB, m0);
         bulk_commit_and_wait_read();  // the boxes are read out before the CTA lets go of its shared memory
     }
+    // After the exchange barrier no CTA reads or writes a peer's shared memory, so the CTAs
+    // of a cluster leave independently; this barrier orders the TMEM reads before the dealloc.
     tc_fence_before();
-    // No CTA leaves while a peer of its cluster may still read or write it.
-    cluster_sync_all();
+    __syncthreads();
     if (warp == 0) {
         // After a timeout, give in-flight MMAs a second bounded wait before the
         // accumulator columns are released.
