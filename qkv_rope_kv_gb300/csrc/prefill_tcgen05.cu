@@ -19,16 +19,18 @@
 // parameters), warp 2 lane 0 the X blocks into another (mbarrier transaction
 // counts); warp 1 lane 0 issues tcgen05.mma (kind::f16, bf16 x bf16 -> f32 in
 // TMEM, K = 16 per instruction) and frees stages with tcgen05.commit.  After
-// the K loop each CTA writes its partial sums of every other tile into that
-// tile's CTA (distributed shared memory), and CTA r adds the S partials of tile
-// r in rank order, so the result does not depend on which CTA finishes first.
-// All four warps then run the epilogue of tile r, one token per thread: bias,
-// RoPE (its (cos, sin) computed while the K loop runs), Y through shared memory
-// (128-byte swizzle) and two TMA tensor stores, the token's k/v cache rows as
-// 16-byte stores.  Every wait is bounded; on expiry the kernel flags the device
-// status word, drains in-flight copies and MMAs, frees TMEM and returns.  Two
-// cluster barriers order the exchange; after the second no CTA touches a peer's
-// shared memory, so the CTAs of a cluster leave independently.
+// the K loop each CTA hands its partial sums of every other tile to that tile's
+// CTA through distributed shared memory (S = 2: staged locally and sent as one
+// bulk copy, counted in bytes on the receiver's mbarrier; S = 4: stores into
+// the peers between two cluster barriers), and CTA r adds the S partials of
+// tile r in rank order, so the result does not depend on which CTA finishes
+// first.  All four warps then run the epilogue of tile r, one token per thread:
+// bias, RoPE (its (cos, sin) computed while the K loop runs), Y through shared
+// memory (128-byte swizzle) and two TMA tensor stores, the token's k/v cache
+// rows as 16-byte stores.  Every wait is bounded; on expiry the kernel flags the
+// device status word, drains in-flight copies and MMAs, frees TMEM and returns.
+// Once the exchange is over no CTA touches a peer's shared memory, so the CTAs
+// of a cluster leave independently.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -76,7 +78,7 @@ struct Split {
     static constexpr int kXStages = S == 1 ? 4 : (S == 2 ? 3 : 6);
     static constexpr int kWStages = static_cast<int>((kRingBytes - kXStages * kXStage) / kWStage);
     static constexpr size_t kSmem = 1024 /* alignment slack */ + kXStages * kXStage + kWStages * kWStage +
-                                    (2 * kXStages + 2 * kWStages + 1) * sizeof(uint64_t) + 16;
+                                    (2 * kXStages + 2 * kWStages + 4) * sizeof(uint64_t) + 16;
     static_assert(kXStages * kXStage + kWStages * kWStage <= kRingBytes, "rings");
     static_assert(kSmem <= 227 * 1024, "prefill rings exceed shared memory");
     // after the K loop the rings hold S exchange slots and the Y staging boxes
@@ -139,6 +141,38 @@ __device__ __forceinline__ uint32_t map_to_rank(const void* p, uint32_t rank) {
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
     return r;
+}
+
+// Remote arrive (release, cluster scope) on an mbarrier at a shared::cluster address.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Bounded wait with cluster-scope acquire (the arrival came from a peer CTA).
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+    }
+}
+
+// Bulk copy of `bytes` from this CTA's shared memory to a peer's (shared::cluster address),
+// completion counted in bytes on the peer's mbarrier.
+__device__ __forceinline__ void bulk_s2cluster(uint32_t dst_cluster, const void* src, uint32_t bytes,
+                                               uint32_t bar_cluster) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst_cluster),
+                 "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
+                 : "memory");
 }
 
 __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
@@ -311,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* wfull = xempty + C::kXStages;
     uint64_t* wempty = wfull + C::kWStages;
     uint64_t* done = wempty + C::kWStages;
+    uint64_t* xb = done + 1;  // exchange: [0] peer idle, [1] peer's copy in, [2] own copy landed
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.y * kBM;
@@ -339,7 +374,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&wempty[s], 1);
         }
         mbar_init(done, 1);
+        mbar_init(&xb[0], 1);
+        mbar_init(&xb[1], 1);
+        mbar_init(&xb[2], 1);
         mbar_fence_init();
+        if (S == 2) mbar_arrive_expect_tx(&xb[1], kXchgSlot);
     }
     if (threadIdx.x < kBox) bias_s[threadIdx.x] = p.bias[own.base + own.rowA + threadIdx.x];
     else if (threadIdx.x < 2 * kBox) bias_s[threadIdx.x] = p.bias[own.base + own.rowB + threadIdx.x - kBox];
@@ -472,7 +511,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     float* xchg = reinterpret_cast<float*>(smem);  // S slots of [128 tokens x kXchgStride], after the K loop
-    if constexpr (S > 1) {
+    float aa[kPc], ab[kPc];  // this thread's pairs: box A and box B values
+    if constexpr (S == 2) {
+        const uint32_t q = rank ^ 1u;
+        float* mine = xchg + rank * kBM * kXchgStride;  // this CTA's partial of tile q, staged locally
+        if (acc_ready) {
+            float va[kPc], vb[kPc];
+            tc_ld_cols<kPc>(taddr + tile_col_a<BLOCK>(static_cast<int>(q), own.sec, p.hd) + c0, va);
+            tc_ld_cols<kPc>(taddr + tile_col_b<BLOCK>(static_cast<int>(q), own.sec, p.hd) + c0, vb);
+            tc_ld_cols<kPc>(taddr + tile_col_a<BLOCK>(static_cast<int>(rank), own.sec, p.hd) + c0, aa);
+            tc_ld_cols<kPc>(taddr + tile_col_b<BLOCK>(static_cast<int>(rank), own.sec, p.hd) + c0, ab);
+            tc_wait_ld();
+            float* d = mine + tl * kXchgStride;
+#pragma unroll
+            for (int c = 0; c < kPc; c += 4) {
+                *reinterpret_cast<float4*>(d + c0 + c) = make_float4(va[c], va[c + 1], va[c + 2], va[c + 3]);
+                *reinterpret_cast<float4*>(d + kBox + c0 + c) = make_float4(vb[c], vb[c + 1], vb[c + 2], vb[c + 3]);
+            }
+        }
+        fence_proxy_async_smem();  // the staged partial is read by the bulk copy
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            // This CTA's rings are idle: the peer may copy into slot q here.
+            mbar_arrive_remote(map_to_rank(&xb[0], q));
+            if (mbar_wait_cluster_bounded(&xb[0], 0))
+                bulk_s2cluster(map_to_rank(mine, q), mine, kXchgSlot, map_to_rank(&xb[1], q));
+            else
+                flag_timeout();
+        }
+        // The peer's partial of this CTA's tile, in slot q (the copy's bytes complete xb[1]).
+        const bool got = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&xb[1], 0));
+        if (!got && lane == 0) flag_timeout();
+        if (threadIdx.x == 0) mbar_arrive_remote(map_to_rank(&xb[2], q));  // the peer's copy has landed
+    } else if constexpr (S > 1) {
         // Every CTA of the cluster is past its K loop before any ring is overwritten.
         tc_fence_before();
         cluster_sync_all();
@@ -497,11 +568,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The partial sums of every peer have landed in this CTA's slots.
         cluster_sync_all();
     }
-    float aa[kPc], ab[kPc];  // this thread's pairs: box A and box B values
     if (acc_ready) {
-        tc_ld_cols<kPc>(taddr + tile_col_a<BLOCK>(static_cast<int>(rank), own.sec, p.hd) + c0, aa);
-        tc_ld_cols<kPc>(taddr + tile_col_b<BLOCK>(static_cast<int>(rank), own.sec, p.hd) + c0, ab);
-        tc_wait_ld();
+        if constexpr (S != 2) {
+            tc_ld_cols<kPc>(taddr + tile_col_a<BLOCK>(static_cast<int>(rank), own.sec, p.hd) + c0, aa);
+            tc_ld_cols<kPc>(taddr + tile_col_b<BLOCK>(static_cast<int>(rank), own.sec, p.hd) + c0, ab);
+            tc_wait_ld();
+        }
         if constexpr (S > 1) {
             // Sum the S K ranges in rank order (the same order in every CTA).
             float sa[kPc], sb[kPc];
@@ -602,8 +674,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_store_2d(&tm_y, ys + kBM * kBox, own.base + own.rowB, m0);
         bulk_commit_and_wait_read();  // the boxes are read out before the CTA lets go of its shared memory
     }
-    // After the exchange barrier no CTA reads or writes a peer's shared memory, so the CTAs
-    // of a cluster leave independently; this barrier orders the TMEM reads before the dealloc.
+    // Once the exchange is over no CTA reads or writes a peer's shared memory, so the CTAs of a
+    // cluster leave independently (S == 2: after the peer reports that this CTA's copy landed,
+    // so the staged source outlives the copy); the barrier orders the TMEM reads before the dealloc.
+    if (S == 2 && threadIdx.x == 0 && !mbar_wait_cluster_bounded(&xb[2], 0)) flag_timeout();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
