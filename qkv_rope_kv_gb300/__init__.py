@@ -137,6 +137,7 @@ def _declare(lib):
         "qkv_model_graph_destroy": ([vp], None),
         "qkv_check_device_error": ([vp, ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(i32)], st),
         "qkv_test_decode_wait_timeout": ([vp] * 10 + [ctypes.c_uint32, vp], st),
+        "qkv_test_prefill_xchg_timeout": ([vp, vp, ctypes.c_int32] + [vp] * 6 + [ctypes.c_uint32, vp], st),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -229,6 +230,15 @@ def qkv_test_decode_wait_timeout(plan: Plan, x, w, bias, d_pos, q, k, v, kv_k, k
     _check(_lib.qkv_test_decode_wait_timeout(plan.handle, _ptr(x), _ptr(w), _ptr(bias), _ptr(d_pos), _ptr(q),
                                              _ptr(k), _ptr(v), _ptr(kv_k), _ptr(kv_v), int(wait_limit_us),
                                              _stream(stream)))
+
+
+def qkv_test_prefill_xchg_timeout(plan: Plan, X, nt: int, w, bias, d_positions, Y, kv_k, kv_v,
+                                  wait_limit_us: int = 200, stream=None):
+    """Test hook (include/qkv_test.h): qkv_prefill_step with the exchange of partial sums
+    withheld and every wait limited to wait_limit_us, so the device status flag 2 gets set."""
+    _check(_lib.qkv_test_prefill_xchg_timeout(plan.handle, _ptr(X), int(nt), _ptr(w), _ptr(bias),
+                                              _ptr(d_positions), _ptr(Y), _ptr(kv_k), _ptr(kv_v),
+                                              int(wait_limit_us), _stream(stream)))
 
 
 def qkv_decode_step_rmsnorm(plan: Plan, h, norm_w, norm_eps: float, w, bias, d_pos, q, k, v, kv_k, kv_v,

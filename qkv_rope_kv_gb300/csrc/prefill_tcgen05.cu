@@ -149,7 +149,7 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
 }
 
 // Bounded wait with cluster-scope acquire (the arrival came from a peer CTA).
-__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
         uint32_t ok;
@@ -161,7 +161,7 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_
             : "r"(smem_u32(bar)), "r"(parity)
             : "memory");
         if (ok) return true;
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 
@@ -349,6 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.y * kBM;
+    const uint64_t limit = p.wait_limit_ns ? p.wait_limit_ns : kWaitTimeoutNs;
     const uint32_t rank = S > 1 ? cluster_rank() : 0u;
     // this CTA's K range, in 64-wide blocks, and the pair tiles of its cluster
     const int nkb = (p.H + kBK - 1) / kBK;
@@ -410,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int issued = 0;
         for (int st = 0; st < n_stages; ++st) {
             const int s = st % C::kWStages;
-            if (st >= C::kWStages && !mbar_wait_bounded(&wempty[s], ((st / C::kWStages) - 1) & 1)) {
+            if (st >= C::kWStages && !mbar_wait_bounded(&wempty[s], ((st / C::kWStages) - 1) & 1, limit)) {
                 flag_timeout();
                 break;
             }
@@ -438,8 +439,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Drain: every W copy has landed and the MMAs released the last stages.
         const int first = issued > C::kWStages ? issued - C::kWStages : 0;
         for (int st = first; st < issued; ++st) {
-            if (!mbar_wait_bounded(&wfull[st % C::kWStages], (st / C::kWStages) & 1)) flag_timeout();
-            if (!mbar_wait_bounded(&wempty[st % C::kWStages], (st / C::kWStages) & 1)) flag_timeout();
+            if (!mbar_wait_bounded(&wfull[st % C::kWStages], (st / C::kWStages) & 1, limit)) flag_timeout();
+            if (!mbar_wait_bounded(&wempty[st % C::kWStages], (st / C::kWStages) & 1, limit)) flag_timeout();
         }
         griddep_wait();  // before this thread writes its epilogue rows
     } else if (warp == 2 && lane == 0) {
@@ -448,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int issued = 0;
         for (int st = 0; st < n_stages; ++st) {
             const int s = st % C::kXStages;
-            if (st >= C::kXStages && !mbar_wait_bounded(&xempty[s], ((st / C::kXStages) - 1) & 1)) {
+            if (st >= C::kXStages && !mbar_wait_bounded(&xempty[s], ((st / C::kXStages) - 1) & 1, limit)) {
                 flag_timeout();
                 break;
             }
@@ -461,15 +462,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int first = issued > C::kXStages ? issued - C::kXStages : 0;
         for (int st = first; st < issued; ++st) {
-            if (!mbar_wait_bounded(&xfull[st % C::kXStages], (st / C::kXStages) & 1)) flag_timeout();
-            if (!mbar_wait_bounded(&xempty[st % C::kXStages], (st / C::kXStages) & 1)) flag_timeout();
+            if (!mbar_wait_bounded(&xfull[st % C::kXStages], (st / C::kXStages) & 1, limit)) flag_timeout();
+            if (!mbar_wait_bounded(&xempty[st % C::kXStages], (st / C::kXStages) & 1, limit)) flag_timeout();
         }
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer: D[128 x 64 S] += X block * (S tiles' W block)^T ----
         for (int st = 0; st < n_stages; ++st) {
             const int xs = st % C::kXStages, ws = st % C::kWStages;
-            if (!mbar_wait_bounded(&xfull[xs], (st / C::kXStages) & 1) ||
-                !mbar_wait_bounded(&wfull[ws], (st / C::kWStages) & 1)) {
+            if (!mbar_wait_bounded(&xfull[xs], (st / C::kXStages) & 1, limit) ||
+                !mbar_wait_bounded(&wfull[ws], (st / C::kWStages) & 1, limit)) {
                 flag_timeout();
                 break;
             }
@@ -506,12 +507,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
     // Warp-uniform: tcgen05.ld below is a warp-collective instruction.
-    const bool acc_ready = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(done, 0));
+    const bool acc_ready = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(done, 0, limit));
     if (!acc_ready && lane == 0) flag_timeout();
     tc_fence_after();
     const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     float* xchg = reinterpret_cast<float*>(smem);  // S slots of [128 tokens x kXchgStride], after the K loop
     float aa[kPc], ab[kPc];  // this thread's pairs: box A and box B values
+    bool ready = acc_ready;  // the accumulator and, for S == 2, the peer's partial are in
     if constexpr (S == 2) {
         const uint32_t q = rank ^ 1u;
         float* mine = xchg + rank * kBM * kXchgStride;  // this CTA's partial of tile q, staged locally
@@ -534,14 +536,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (threadIdx.x == 0) {
             // This CTA's rings are idle: the peer may copy into slot q here.
             mbar_arrive_remote(map_to_rank(&xb[0], q));
-            if (mbar_wait_cluster_bounded(&xb[0], 0))
-                bulk_s2cluster(map_to_rank(mine, q), mine, kXchgSlot, map_to_rank(&xb[1], q));
-            else
+            if (!mbar_wait_cluster_bounded(&xb[0], 0, limit))
                 flag_timeout();
+            else if (!p.withhold_xchg)
+                bulk_s2cluster(map_to_rank(mine, q), mine, kXchgSlot, map_to_rank(&xb[1], q));
         }
         // The peer's partial of this CTA's tile, in slot q (the copy's bytes complete xb[1]).
-        const bool got = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&xb[1], 0));
+        // Without it the tile is not written.
+        const bool got = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&xb[1], 0, limit));
         if (!got && lane == 0) flag_timeout();
+        ready = ready && got;
         if (threadIdx.x == 0) mbar_arrive_remote(map_to_rank(&xb[2], q));  // the peer's copy has landed
     } else if constexpr (S > 1) {
         // Every CTA of the cluster is past its K loop before any ring is overwritten.
@@ -568,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The partial sums of every peer have landed in this CTA's slots.
         cluster_sync_all();
     }
-    if (acc_ready) {
+    if (ready) {
         if constexpr (S != 2) {
             tc_ld_cols<kPc>(taddr + tile_col_a<BLOCK>(static_cast<int>(rank), own.sec, p.hd) + c0, aa);
             tc_ld_cols<kPc>(taddr + tile_col_b<BLOCK>(static_cast<int>(rank), own.sec, p.hd) + c0, ab);
@@ -603,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- epilogue of this CTA's tile ----
     float* ys = xchg + S * (kXchgSlot / 4);  // Y staging, past the exchange slots
-    if (acc_ready) {
+    if (ready) {
         const bool live = t < p.nt;
         const bool store = live && pos_ok(pos, p.n_ctx);
         if (live && !store && c0 == 0) flag_bad_pos(pos);
@@ -668,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_proxy_async_smem();
     // Every warp has staged its rows (or the accumulator never became ready).
-    const bool tile_ready = __syncthreads_and(acc_ready) != 0;
+    const bool tile_ready = __syncthreads_and(ready) != 0;
     if (tile_ready && threadIdx.x == 0) {
         tma_store_2d(&tm_y, ys, own.base + own.rowA, m0);
         tma_store_2d(&tm_y, ys + kBM * kBox, own.base + own.rowB, m0);
@@ -677,13 +681,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Once the exchange is over no CTA reads or writes a peer's shared memory, so the CTAs of a
     // cluster leave independently (S == 2: after the peer reports that this CTA's copy landed,
     // so the staged source outlives the copy); the barrier orders the TMEM reads before the dealloc.
-    if (S == 2 && threadIdx.x == 0 && !mbar_wait_cluster_bounded(&xb[2], 0)) flag_timeout();
+    if (S == 2 && threadIdx.x == 0 && !mbar_wait_cluster_bounded(&xb[2], 0, limit)) flag_timeout();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
         // After a timeout, give in-flight MMAs a second bounded wait before the
         // accumulator columns are released.
-        if (!acc_ready) mbar_wait_bounded(done, 0);
+        if (!acc_ready) mbar_wait_bounded(done, 0, limit);
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(static_cast<uint32_t>(C::kN))
@@ -795,6 +799,10 @@ qkv_status launch_prefill(const PrefillParams& p, bool pdl, cudaStream_t stream,
     const int nkb = (p.H + kBK - 1) / kBK;
     int split = QKV_PREFILL_SPLIT;
     while (split > 1 && (tiles % split != 0 || nkb < split)) split >>= 1;
+    if (p.withhold_xchg && split != 2) {
+        *why = "the exchange-timeout test needs clusters of 2 (an even count of 64-row tiles and H > 64)";
+        return QKV_ERR_UNSUPPORTED;
+    }
     // One 16 KB W box per K block and cluster (in place of four 4 KB boxes) when the cluster's
     // two pair tiles are 128 consecutive rows: whole heads of 64 or 128 rows, and no cluster
     // across the q|k or k|v boundary.  A bulk tensor load costs about the same time whatever

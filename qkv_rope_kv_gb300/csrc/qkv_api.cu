@@ -491,7 +491,7 @@ qkv_status check_prefill(const qkv_plan* plan, int32_t nt, const uint16_t* X, co
 
 qkv_status run_prefill(const qkv_plan* plan, const uint16_t* X, int32_t nt, const void* w, const float* bias,
                        const int32_t* d_positions, float* Y, void* kv_k, void* kv_v, bool pdl,
-                       cudaStream_t stream) {
+                       cudaStream_t stream, uint64_t wait_limit_ns = 0, int32_t withhold_xchg = 0) {
     if (nt == 0) return QKV_OK;
     PrefillParams p;
     std::memset(&p, 0, sizeof p);
@@ -509,6 +509,8 @@ qkv_status run_prefill(const qkv_plan* plan, const uint16_t* X, int32_t nt, cons
     p.hd = plan->d.head_dim;
     p.n_ctx = plan->d.n_ctx;
     p.kv_f16 = plan->d.kv_dtype == QKV_F16 ? 1 : 0;
+    p.wait_limit_ns = wait_limit_ns;
+    p.withhold_xchg = withhold_xchg;
     std::memcpy(p.inv_freq, plan->inv_freq, sizeof p.inv_freq);
     const char* why = nullptr;
     qkv_status st = launch_prefill(p, pdl, stream, &why);
@@ -525,6 +527,19 @@ extern "C" qkv_status qkv_prefill_step(const qkv_plan* plan, const uint16_t* X, 
     qkv_status st = check_prefill(plan, nt, X, w, bias, d_positions, Y, kv_k, kv_v);
     if (st != QKV_OK) return st;
     return run_prefill(plan, X, nt, w, bias, d_positions, Y, kv_k, kv_v, false, static_cast<cudaStream_t>(stream));
+}
+
+// Test hook (include/qkv_test.h): the prefill's exchange wait made to run out.
+extern "C" qkv_status qkv_test_prefill_xchg_timeout(const qkv_plan* plan, const uint16_t* X, int32_t nt,
+                                                    const void* w, const float* bias, const int32_t* d_positions,
+                                                    float* Y, void* kv_k, void* kv_v, uint32_t wait_limit_us,
+                                                    void* stream) {
+    REQUIRE(wait_limit_us >= 1 && wait_limit_us <= 1000, "wait_limit_us must be in [1, 1000]");
+    qkv_status st = check_prefill(plan, nt, X, w, bias, d_positions, Y, kv_k, kv_v);
+    if (st != QKV_OK) return st;
+    REQUIRE(nt >= 1, "nt must be >= 1");
+    return run_prefill(plan, X, nt, w, bias, d_positions, Y, kv_k, kv_v, false, static_cast<cudaStream_t>(stream),
+                       1000ull * wait_limit_us, 1);
 }
 
 // ------------------------------------------------------------------ FusedFFN

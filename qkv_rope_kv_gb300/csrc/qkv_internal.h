@@ -79,6 +79,11 @@ struct PrefillParams {
     void* kv_k;
     void* kv_v;
     int32_t nt, H, nqt, nkt, hd, n_ctx, kv_f16;
+    // Test hook of the bounded waits (zero in every product call): a non-zero wait limit
+    // replaces the default, and withhold_xchg makes each CTA of a cluster of 2 skip sending its
+    // partial sums to the peer, so the peer's wait for them runs out.
+    unsigned long long wait_limit_ns;
+    int32_t withhold_xchg;
     float inv_freq[QKV_MAX_HEAD_DIM / 2];
 };
 qkv_status launch_prefill(const PrefillParams& p, bool pdl, cudaStream_t stream, const char** why);

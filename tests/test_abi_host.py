@@ -324,3 +324,19 @@ def test_wait_timeout_hook_guards(lib):
     st = lib.qkv_test_decode_wait_timeout(plan.handle, None, fake, fake, fake, fake, fake, fake, fake, fake, 100,
                                           None)
     assert st == q.QKV_ERR_INVALID_ARG and b"x is null" in lib.qkv_last_error()
+
+
+def test_prefill_xchg_timeout_hook_guards(lib):
+    """The prefill failure-path hook rejects a wait limit outside 1 .. 1000 us, null pointers and
+    a shape that does not run on clusters of 2 (an odd number of 64-row tiles), before any CUDA
+    call."""
+    fake = 16 * 64
+    plan = q.qkv_plan_create(256, 4, 2, 64, 1e4, 8, w_dtype=q.QKV_BF16)  # R = 512: 8 tiles
+    for us in (0, 1001):
+        st = lib.qkv_test_prefill_xchg_timeout(plan.handle, fake, 4, fake, fake, fake, fake, fake, fake, us, None)
+        assert st == q.QKV_ERR_INVALID_ARG and b"wait_limit_us" in lib.qkv_last_error()
+    st = lib.qkv_test_prefill_xchg_timeout(plan.handle, None, 4, fake, fake, fake, fake, fake, fake, 100, None)
+    assert st == q.QKV_ERR_INVALID_ARG and b"null pointer" in lib.qkv_last_error()
+    odd = q.qkv_plan_create(256, 1, 1, 64, 1e4, 8, w_dtype=q.QKV_BF16)  # R = 192: 3 tiles
+    st = lib.qkv_test_prefill_xchg_timeout(odd.handle, fake, 4, fake, fake, fake, fake, fake, fake, 100, None)
+    assert st == q.QKV_ERR_UNSUPPORTED and b"clusters of 2" in lib.qkv_last_error()

@@ -1,4 +1,5 @@
-"""The device-side failure path of the decode rings, made to happen without a GPU fault.
+"""The device-side failure paths of the decode rings and of the prefill, made to happen
+without a GPU fault.
 
 Every wait of a ring kernel on a pipeline barrier is bounded.  The test hook
 qkv_test_decode_wait_timeout (include/qkv_test.h) withholds the last weight copy of
@@ -8,6 +9,11 @@ flag (2), no cache row other than the step's position may change, and the next
 ordinary call on the same context must match the oracle.  Shapes cover the three ring
 shapes: the block ring (rows of 8 KB), the pair ring (4-8 KB rows) and the short-row
 pair ring (rows under 4 KB, f32 weights).
+
+qkv_test_prefill_xchg_timeout withholds the prefill's exchange of partial sums between
+the two CTAs of each cluster (the two K halves of a 128-row block), so every CTA's wait
+for its peer's partial runs out: the flag must be set, no Y row and no cache row may be
+written, and the next ordinary prefill must match the oracle.
 """
 import time
 
@@ -67,3 +73,47 @@ def test_withheld_copy_times_out_and_context_stays_usable(orc, qkv, shape):
     assert_f32_close(got[b:], v, "after timeout v")
     assert_kv_region(to_host(dk, np.uint16), kk, pos, "after timeout K", section_f32=k)
     assert_kv_region(to_host(dv, np.uint16), vv, pos, "after timeout V", section_f32=v)
+
+
+PREFILL_SHAPES = [
+    # H, nh, nkv, hd, nt, kv dtype: heads of 64 (clusters span two heads), heads of 128 with two token tiles
+    (1024, 4, 2, 64, 40, "f16"),
+    (640, 2, 1, 128, 130, "f32"),
+]
+
+
+@pytest.mark.parametrize("shape", PREFILL_SHAPES, ids=lambda s: "H%d_d%d_nt%d_%s" % (s[0], s[3], s[4], s[5]))
+def test_prefill_withheld_exchange_times_out_and_context_stays_usable(orc, qkv, shape):
+    import torch
+    from qkv_rope_kv_gb300 import synth
+    from test_prefill_gpu import DT, check, oracle_prefill, run_prefill
+    H, nh, nkv, hd, nt, kvdt = shape
+    n_ctx = nt + 10
+    R = (nh + 2 * nkv) * hd
+    W = synth.weight_rows(0, 5, 0, R, H, "bf16")
+    b = synth.bias(0, 5, R)
+    X = synth.prefill_x(0, 5, nt, H)
+    positions = np.random.default_rng(nt + H).permutation(n_ctx)[:nt].astype(np.int32)
+    kk0, vv0 = canary(n_ctx, nkv * hd, kvdt, 81), canary(n_ctx, nkv * hd, kvdt, 82)
+    plan = Q.qkv_plan_create(H, nh, nkv, hd, 1e6, n_ctx, w_dtype=Q.QKV_BF16, kv_dtype=DT[kvdt])
+    dY = torch.full((nt, R), float("nan"), dtype=torch.float32, device="cuda")
+    dk, dv = to_dev(kk0), to_dev(vv0)
+    dpos = torch.from_numpy(positions).cuda()
+    Q.qkv_check_device_error()
+    t0 = time.perf_counter()
+    Q.qkv_test_prefill_xchg_timeout(plan, to_dev(X), nt, to_dev(W), to_dev(b), dpos, dY, dk, dv, wait_limit_us=200)
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 < 10.0
+    flags, _ = Q.qkv_check_device_error()
+    assert flags & 2, "no timeout flag after a withheld exchange (flags %#x)" % flags
+    # no CTA received its peer's partial: no Y row and no cache row was written
+    assert np.isnan(to_host(dY)).all()
+    bits = np.uint32 if kvdt == "f32" else np.uint16
+    assert np.array_equal(to_host(dk, bits), kk0.view(bits))
+    assert np.array_equal(to_host(dv, bits), vv0.view(bits))
+
+    # the context is usable: an ordinary prefill matches the per-token oracle
+    got = run_prefill(H, nh, nkv, hd, n_ctx, kvdt, X, W, b, positions, kk0, vv0)
+    assert Q.qkv_check_device_error()[0] == 0
+    want = oracle_prefill(orc, X, W, b, positions, nh, nkv, hd, kk0, vv0)
+    check(nh, nkv, hd, got, want, positions, "prefill after timeout")
