@@ -20,11 +20,10 @@
 // counts); warp 1 lane 0 issues tcgen05.mma (kind::f16, bf16 x bf16 -> f32 in
 // TMEM, K = 16 per instruction) and frees stages with tcgen05.commit.  After
 // the K loop each CTA hands its partial sums of every other tile to that tile's
-// CTA through distributed shared memory (S = 2: staged locally and sent as one
-// bulk copy, counted in bytes on the receiver's mbarrier; S = 4: stores into
-// the peers between two cluster barriers), and CTA r adds the S partials of
-// tile r in rank order, so the result does not depend on which CTA finishes
-// first.  All four warps then run the epilogue of tile r, one token per thread:
+// CTA through distributed shared memory (staged locally and sent as one bulk
+// copy, counted in bytes on the receiver's mbarrier), and CTA r adds the S
+// partials of tile r in rank order, so the result does not depend on which CTA
+// finishes first.  All four warps then run the epilogue of tile r, one token per thread:
 // bias, RoPE (its (cos, sin) computed while the K loop runs), Y through shared
 // memory (128-byte swizzle) and two TMA tensor stores, the token's k/v cache
 // rows as 16-byte stores.  Every wait is bounded; on expiry the kernel flags the
@@ -70,12 +69,13 @@ constexpr uint32_t kXchgSlot = kBM * kXchgStride * 4;
 // of all S tiles.  kSub 64-wide K blocks form a stage.
 template <int S>
 struct Split {
+    static_assert(S == 1 || S == 2, "clusters of 1 or 2 CTAs");
     static constexpr int kN = kBN * S;                        // UMMA N and TMEM columns
-    static constexpr int kSub = S >= 4 ? 1 : 2;
+    static constexpr int kSub = 2;
     static constexpr uint32_t kXStage = kSub * kABlk;
     static constexpr uint32_t kWBlk = S * kTileBlk;           // W bytes of one K block
     static constexpr uint32_t kWStage = kSub * kWBlk;
-    static constexpr int kXStages = S == 1 ? 4 : (S == 2 ? 3 : 6);
+    static constexpr int kXStages = S == 1 ? 4 : 3;
     static constexpr int kWStages = static_cast<int>((kRingBytes - kXStages * kXStage) / kWStage);
     static constexpr size_t kSmem = 1024 /* alignment slack */ + kXStages * kXStage + kWStages * kWStage +
                                     (2 * kXStages + 2 * kWStages + 4) * sizeof(uint64_t) + 16;
@@ -172,11 +172,6 @@ __device__ __forceinline__ void bulk_s2cluster(uint32_t dst_cluster, const void*
     asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      dst_cluster),
                  "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
-                 : "memory");
-}
-
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                  : "memory");
 }
 
@@ -547,33 +542,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!got && lane == 0) flag_timeout();
         ready = ready && got;
         if (threadIdx.x == 0) mbar_arrive_remote(map_to_rank(&xb[2], q));  // the peer's copy has landed
-    } else if constexpr (S > 1) {
-        // Every CTA of the cluster is past its K loop before any ring is overwritten.
-        tc_fence_before();
-        cluster_sync_all();
-        tc_fence_after();
-        if (acc_ready) {
-            // Send this CTA's partial sums of tile q to CTA q, into slot `rank` there.
-#pragma unroll 1
-            for (int q = 0; q < S; ++q) {
-                if (q == static_cast<int>(rank)) continue;
-                float va[kPc], vb[kPc];
-                tc_ld_cols<kPc>(taddr + tile_col_a<BLOCK>(q, own.sec, p.hd) + c0, va);
-                tc_ld_cols<kPc>(taddr + tile_col_b<BLOCK>(q, own.sec, p.hd) + c0, vb);
-                tc_wait_ld();
-                const uint32_t dst = map_to_rank(xchg + (rank * kBM + tl) * kXchgStride, static_cast<uint32_t>(q));
-#pragma unroll
-                for (int c = 0; c < kPc; c += 4) {
-                    st_cluster_v4(dst + (c0 + c) * 4, va[c], va[c + 1], va[c + 2], va[c + 3]);
-                    st_cluster_v4(dst + (kBox + c0 + c) * 4, vb[c], vb[c + 1], vb[c + 2], vb[c + 3]);
-                }
-            }
-        }
-        // The partial sums of every peer have landed in this CTA's slots.
-        cluster_sync_all();
     }
     if (ready) {
-        if constexpr (S != 2) {
+        if constexpr (S == 1) {
             tc_ld_cols<kPc>(taddr + tile_col_a<BLOCK>(static_cast<int>(rank), own.sec, p.hd) + c0, aa);
             tc_ld_cols<kPc>(taddr + tile_col_b<BLOCK>(static_cast<int>(rank), own.sec, p.hd) + c0, ab);
             tc_wait_ld();
@@ -791,14 +762,11 @@ qkv_status launch_prefill(const PrefillParams& p, bool pdl, cudaStream_t stream,
     }
     const int R = p.nqt + 2 * p.nkt;
     const int tiles = R / kBN;
-    // Cluster of S pair tiles splitting K: the largest of 4, 2, 1 that divides the
-    // tiles and leaves every CTA at least one 64-wide K block.
-#ifndef QKV_PREFILL_SPLIT
-#define QKV_PREFILL_SPLIT 2
-#endif
+    // Clusters of 2 pair tiles splitting K in halves when the tile count is even and K has at
+    // least two 64-wide blocks, else one CTA per pair tile over the whole K range.  (Clusters
+    // of 4 splitting K in quarters measured slower and are not built.)
     const int nkb = (p.H + kBK - 1) / kBK;
-    int split = QKV_PREFILL_SPLIT;
-    while (split > 1 && (tiles % split != 0 || nkb < split)) split >>= 1;
+    const int split = tiles % 2 == 0 && nkb >= 2 ? 2 : 1;
     if (p.withhold_xchg && split != 2) {
         *why = "the exchange-timeout test needs clusters of 2 (an even count of 64-row tiles and H > 64)";
         return QKV_ERR_UNSUPPORTED;
@@ -818,9 +786,7 @@ qkv_status launch_prefill(const PrefillParams& p, bool pdl, cudaStream_t stream,
         return QKV_ERR_CUDA;
     }
     cudaError_t e;
-    if (split == 4)
-        e = launch_split<4>(tm_x, tm_w, tm_y, p, tiles, pdl, stream);
-    else if (split == 2 && block)
+    if (split == 2 && block)
         e = launch_split<2, true>(tm_x, tm_w, tm_y, p, tiles, pdl, stream);
     else if (split == 2)
         e = launch_split<2>(tm_x, tm_w, tm_y, p, tiles, pdl, stream);
