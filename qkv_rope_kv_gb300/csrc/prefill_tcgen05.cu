@@ -15,10 +15,10 @@
 // tiles and splits K (64-wide blocks, 128 bytes: one 128B-swizzle row) into S
 // ranges: each CTA multiplies its K range of X by the W rows of all S tiles
 // (one UMMA with N = 64 S), so it stages 1/S of X per weight row.  Warp 0 lane 0
-// streams W boxes into its ring (before the dependency wait: weights are
-// parameters), warp 2 lane 0 the X blocks into another (mbarrier transaction
-// counts); warp 1 lane 0 issues tcgen05.mma (kind::f16, bf16 x bf16 -> f32 in
-// TMEM, K = 16 per instruction) and frees stages with tcgen05.commit.  After
+// streams W boxes into its ring, warp 2 lane 0 the X blocks into another (mbarrier
+// transaction counts), both after the dependency wait; warp 1 lane 0 issues
+// tcgen05.mma (kind::f16, bf16 x bf16 -> f32 in TMEM, K = 16 per instruction) and
+// frees stages with tcgen05.commit.  After
 // the K loop each CTA hands its partial sums of every other tile to that tile's
 // CTA through distributed shared memory (staged locally and sent as one bulk
 // copy, counted in bytes on the receiver's mbarrier), and CTA r adds the S
@@ -385,19 +385,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = tmem_slot;
     // The next grid may be scheduled now (it waits for this one before it reads
     // anything this one writes).  X, positions and the outputs may belong to the
-    // preceding grid in the stream: every thread waits for it before touching
-    // them.  Weights are parameters, so the W producer streams them first.
+    // preceding grid in the stream: every thread waits for it before touching them.
+    // The W stream waits too, although weights are parameters: the next layer's CTAs
+    // that land on SMs this layer leaves idle start when this layer starts, and their
+    // W copies issued at once (a dedicated producer warp that does not wait) compete
+    // with this layer's first stages and cost 3 % per layer.
     griddep_launch_dependents();
-    if (!(warp == 0 && lane == 0)) griddep_wait();
+    griddep_wait();
 
     if (warp == 0 && lane == 0) {
         // ---- W producer: per K block, the two 32-row boxes of each of the S pair tiles ----
         prefetch_tensormap(&tm_w);
         {
-            // Warm L2 with this cluster's share of the X rows in this CTA's K range (every X
-            // block is read by all clusters at about the same time, so its first reads would
-            // otherwise wait for HBM together).  A prefetch binds no values: the X loads after
-            // the dependency wait still read what the preceding grid wrote.
+            // Warm L2 with this cluster's share of the X rows in this CTA's K range: every
+            // cluster reads each X block at about the same time, so its first reads would
+            // otherwise wait for HBM together.
             const int k_lo = kb_lo * kBK, k_n = min(kb_hi * kBK, p.H) - k_lo;
             const int ncl = static_cast<int>(gridDim.x) / S, cl = static_cast<int>(blockIdx.x) / S;
             for (int t = m0 + cl; t < min(m0 + kBM, p.nt); t += ncl)
@@ -437,7 +439,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait_bounded(&wfull[st % C::kWStages], (st / C::kWStages) & 1, limit)) flag_timeout();
             if (!mbar_wait_bounded(&wempty[st % C::kWStages], (st / C::kWStages) & 1, limit)) flag_timeout();
         }
-        griddep_wait();  // before this thread writes its epilogue rows
     } else if (warp == 2 && lane == 0) {
         // ---- X producer: 128 x 64 X blocks of this CTA's K range ----
         prefetch_tensormap(&tm_x);
