@@ -60,3 +60,29 @@ def test_roofline_entry_arithmetic():
     assert abs(e["frac"] - e["hbm_gbs"] / e["peak"]) < 1e-12
     assert abs(e["frac_of_nominal_8000"] - e["hbm_gbs"] / 8000.0) < 1e-12
     assert e["launches_per_step"] == w.n_layers and e["workload"] == w.name
+
+
+def test_direct_step_only_for_one_plain_layer(monkeypatch):
+    """A one-layer decode workload is timed as one qkv_decode_step (or _mixed) launch per step;
+    every multi-layer, sweep or fused-norm workload replays its graph (direct_step is None)."""
+    import dataclasses
+    sys.path.insert(0, ROOT)
+    import bench
+    import qkv_rope_kv_gb300 as Q
+    from qkv_rope_kv_gb300 import configs
+    calls = []
+    monkeypatch.setattr(Q, "qkv_decode_step", lambda *a: calls.append(("concat", len(a))))
+    monkeypatch.setattr(Q, "qkv_decode_step_mixed", lambda *a: calls.append(("mixed", len(a))))
+    w = configs.WORKLOADS["qwen2.5-0.5b-single-layer"]
+    assert w.n_layers == 1
+    layer = dict(x=1, w=2, bias=3, q=4, k=5, v=6, kv_k=7, kv_v=8)
+    m = dict(layers=[layer], layer_plans=["plan"], dpos=9)
+    bench.direct_step(m, w, "stream")()
+    assert calls == [("concat", 11)]
+    mixed = dict(x=1, wq=2, wk=3, wv=4, bias_q=5, bias_k=6, bias_v=7, q=8, k=9, v=10, kv_k=11, kv_v=12)
+    bench.direct_step(dict(m, layers=[mixed]), w, "stream")()
+    assert calls[-1] == ("mixed", 15)
+    for other in (configs.QWEN7B, configs.WORKLOADS["qwen2.5-0.5b-24layer-sweep"],
+                  dataclasses.replace(w, rmsnorm=True), dataclasses.replace(w, qknorm=True),
+                  dataclasses.replace(w, positions=(0, 1))):
+        assert bench.direct_step(m, other, "stream") is None
