@@ -219,7 +219,7 @@ qkv_status qkv_chain_store(const qkv_plan* plan, const float* src, void* cache,
  * X, w, Y, kv_k and kv_v must be 16-byte aligned (TMA operands and 16-byte
  * cache stores).  nt == 0 returns QKV_OK without a launch.  A token whose
  * position lies outside [0, n_ctx) still gets its Y row; its cache rows are not
- * written and the device status flag 1 is set (qkv_check_device_error).
+ * written and bit 0 of the device status flags is set (qkv_check_device_error).
  * Errors: INVALID_ARG (null or misaligned pointers, nt < 0), UNSUPPORTED (f32
  * weights, mixed class, head_dim % 64 != 0, hidden % 8 != 0), CUDA. */
 qkv_status qkv_prefill_step(const qkv_plan* plan, const uint16_t* X, int32_t nt,
